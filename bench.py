@@ -1,0 +1,653 @@
+"""R-SWA benchmark on one GB300 (replicas on N GPUs under torchrun).
+
+Headline workload (single page, bf16): B 1, H 10, d 128, prefix m 288 (256
+visual tokens + 32 prompt), window n 128, T 6000 output tokens.  One step is
+the whole hot path over that input: the prefix prefill (cache write +
+attention over the 288 prefix rows) followed by 6000 fused append+decode
+steps through the ring cache.  Value: output tokens/s.
+
+Extra measurements in the same JSON line (the HBM and tensor-core targets):
+  batched_decode   B 64, m_b ~ U{256..2048}, ring full (T 4096), one step
+  decode_sweep     B 32, m 2600, T in 256 .. 100000: flat per-step latency
+  prefill          B 1, m 10272, T 22496 (32K rows), 12 independent layers
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
+                       [--impl ours|reference] [--no-extras]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("R-SWA decode HBM GB/s & tokens/s vs T; prefill TFLOP/s "
+          "(fraction of GB300 peak)")
+L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "decode_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh"],
+    "prefill_tc_kernel": ["prefill_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
+}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p.get(k, FALLBACK_PEAKS[k])) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sha(name):
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sliding_window_attention_02_gb300", "csrc")
+    for f in KERNEL_SOURCES[name]:
+        p = os.path.join(csrc, f)
+        if os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    sources are unchanged since it was taken; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(name)
+    if not rec or rec.get("source_sha") != kernel_sha(name):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during a timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[3:7]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workloads (setup shared with the full-size GPU tests)
+# ---------------------------------------------------------------------------
+
+def setup_single_page(dev, seed=0, pinned_inputs=False):
+    """Cache and inputs of the single-page workload, plus CUDA graphs for the
+    prefix prefill and the 6000-step fused decode loop."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    B, H, d, m, n, T = w.batch, w.heads, w.head_dim, w.m, w.n, w.T
+    Q, K, V = workloads.qkv(m + T, H, d, seed, w.std, torch.bfloat16, device=dev)
+    cache = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+    Op = torch.empty(m, H, d, dtype=torch.bfloat16, device=dev)
+    Od = torch.empty(T, B, H, d, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    st = {"w": w, "Q": Q, "K": K, "V": V, "cache": cache, "Op": Op, "Od": Od,
+          "stream": s}
+
+    def prefill():
+        cache.prefill(Q[:m], K[:m], V[:m], Op, [m], 0, stream=s)
+
+    def decode_loop():
+        for t in range(T):
+            cache.decode_step_fused(Q[m + t][None], K[m + t][None],
+                                    V[m + t][None], Od[t], stream=s)
+
+    st["prefill"], st["decode_loop"] = prefill, decode_loop
+    with torch.cuda.stream(s):
+        prefill()
+        decode_loop()          # eager run before capture
+    torch.cuda.synchronize(dev)
+    g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=s):
+        prefill()
+    with torch.cuda.graph(g2, stream=s):
+        decode_loop()
+    st["g_prefill"], st["g_decode"] = g1, g2
+    return st
+
+
+def single_page_bytes_per_decode(w):
+    """Algorithmic bytes of one fused decode launch, averaged over the loop:
+    K and V of the m + min(n, t + 1) attended keys for every head, plus q, k,
+    v read and o written."""
+    B, H, d, m, n, T = w.batch, w.heads, w.head_dim, w.m, w.n, w.T
+    keys = sum(m + min(n, t + 1) for t in range(T)) / T
+    return B * H * d * 2 * (2 * keys + 4)
+
+
+def setup_batched(dev, seed=0):
+    """64 sequences with ragged prefixes and a full ring (T = 4096)."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["batched_decode_bf16"]
+    B, H, d, n, T = w.batch, w.heads, w.head_dim, w.n, w.T
+    m_list = workloads.prefix_lengths(B, *w.m_range, seed=seed)
+    rows = sum(m + T for m in m_list)
+    _, K, V = workloads.qkv(rows, H, d, seed, 1.0, torch.bfloat16, device=dev)
+    cache = rswa.RswaCache(w.m_range[1], n, H, d, B, rswa.RSWA_BF16, device=dev)
+    cache.prefill(None, K, V, None, m_list, T)
+    steps = workloads.qkv(64 * B, H, d, seed + 1000, 1.0, torch.bfloat16,
+                          device=dev)
+    return {"w": w, "cache": cache, "m_list": m_list, "K": K, "V": V,
+            "steps": steps}
+
+
+def batched_step_bytes(m_list, w):
+    B, H, d, n = w.batch, w.heads, w.head_dim, w.n
+    keys = sum(m + n for m in m_list)
+    return H * d * 2 * (2 * keys + 4 * B)
+
+
+def setup_sweep(dev, seed=0):
+    """32 sequences, m 2600; ring filled by a prefill of n outputs; t_b is
+    then restored to each swept T (rswa_cache_set_t)."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["decode_sweep_bf16"]
+    B, H, d, m, n = w.batch, w.heads, w.head_dim, w.m, w.n
+    _, K, V = workloads.qkv(B * (m + n), H, d, seed, 1.0, torch.bfloat16,
+                            device=dev)
+    cache = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+    cache.prefill(None, K, V, None, [m] * B, n)
+    steps = workloads.qkv(64 * B, H, d, seed + 2000, 1.0, torch.bfloat16,
+                          device=dev)
+    return {"w": w, "cache": cache, "K": K, "V": V, "steps": steps}
+
+
+def setup_prefill(dev, layers=None, seed0=0):
+    """Multi-page prefill: 12 layers with independent seeded Q/K/V."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["multipage_prefill_bf16"]
+    B, H, d, m, n, T = w.batch, w.heads, w.head_dim, w.m, w.n, w.T
+    layers = w.layers if layers is None else layers
+    L = m + T
+    qkv = [workloads.qkv(L, H, d, seed0 + i, 1.0, torch.bfloat16, device=dev)
+           for i in range(layers)]
+    caches = [rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+              for _ in range(layers)]
+    outs = [torch.empty(L, H, d, dtype=torch.bfloat16, device=dev)
+            for _ in range(layers)]
+    return {"w": w, "qkv": qkv, "caches": caches, "outs": outs}
+
+
+def prefill_flops(w):
+    """4 * d * |visible pairs| * H: QK^T and PV over the R-SWA mask only."""
+    m, n, T, H, d = w.m, w.n, w.T, w.heads, w.head_dim
+    pairs = m * (m + 1) // 2 + T * m + sum(min(n, t + 1) for t in range(T))
+    return 4 * d * pairs * H * w.batch
+
+
+# ---------------------------------------------------------------------------
+# timing
+# ---------------------------------------------------------------------------
+
+def events_time(fn, stream, iters, flush=None):
+    """Mean ms of fn() over iters, CUDA events on `stream`, optional L2 flush
+    between iterations (outside the timed events)."""
+    import torch
+    times = []
+    for _ in range(iters):
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    return times
+
+
+def run_extras(dev, peaks, quick=False):
+    import torch
+    out = {}
+    s = torch.cuda.Stream(device=dev)
+    # batched decode --------------------------------------------------------
+    bt = setup_batched(dev)
+    w = bt["w"]
+    B, H, d = w.batch, w.heads, w.head_dim
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    q, k, v = bt["steps"]
+    idx = [0]
+
+    def bstep():
+        i = idx[0] % 64
+        idx[0] += 1
+        bt["cache"].decode_step_fused(q[i * B:(i + 1) * B], k[i * B:(i + 1) * B],
+                                      v[i * B:(i + 1) * B], o, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            bstep()
+    ts = events_time(bstep, s, 10 if quick else 30)
+    ms = statistics.mean(ts)
+    nbytes = batched_step_bytes(bt["m_list"], w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["batched_decode"] = {
+        "workload": "B64 H10 d128 m~U{256..2048} n128 T4096 bf16, one fused step",
+        "us_per_step": round(ms * 1e3, 2), "tokens_per_s": round(B / (ms * 1e-3), 1),
+        "algorithmic_bytes": nbytes, "GB_per_s": round(gbs, 1),
+        "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+        "l2": "inputs (%.2f GB) larger than L2" % (nbytes / 1e9)}
+    del bt
+    # decode sweep ----------------------------------------------------------
+    sw = setup_sweep(dev)
+    w = sw["w"]
+    B, H, d, m, n = w.batch, w.heads, w.head_dim, w.m, w.n
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    q, k, v = sw["steps"]
+    rows = []
+    nbytes = H * d * 2 * (2 * B * (m + n) + 4 * B)
+    for T in w.T_sweep:
+        sw["cache"].set_t([T] * B)
+        idx = [0]
+
+        def sstep():
+            i = idx[0] % 64
+            idx[0] += 1
+            sw["cache"].decode_step_fused(q[i * B:(i + 1) * B], k[i * B:(i + 1) * B],
+                                          v[i * B:(i + 1) * B], o, stream=s)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                sstep()
+        ts = events_time(sstep, s, 8 if quick else 20)
+        ms = statistics.mean(ts)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"T": T, "us_per_step": round(ms * 1e3, 2),
+                     "GB_per_s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+    us = [r["us_per_step"] for r in rows]
+    out["decode_sweep"] = {
+        "workload": "B32 H10 d128 m2600 n128 bf16, T set by rswa_cache_set_t",
+        "algorithmic_bytes": nbytes, "points": rows,
+        "latency_spread": round((max(us) - min(us)) / statistics.mean(us), 4)}
+    del sw
+    # multi-page prefill ----------------------------------------------------
+    pf = setup_prefill(dev, layers=2 if quick else None)
+    w = pf["w"]
+    layers = len(pf["caches"])
+
+    def pstep():
+        for (Q, K, V), c, O in zip(pf["qkv"], pf["caches"], pf["outs"]):
+            c.prefill(Q, K, V, O, [w.m], w.T, stream=s)
+    with torch.cuda.stream(s):
+        pstep()
+    ts = events_time(pstep, s, 2 if quick else 3)
+    ms = statistics.mean(ts)
+    flops = prefill_flops(w) * layers
+    tf = flops / (ms * 1e-3) / 1e12
+    out["prefill"] = {
+        "workload": "B1 H10 d128 m10272 T22496 (32K) n128 bf16, %d layers" % layers,
+        "ms_per_step": round(ms, 3), "algorithmic_flops": flops,
+        "TFLOP_per_s": round(tf, 1),
+        "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+        "frac_bf16_burst": round(tf / peaks["bf16_tflops"], 4)}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (runs in a subprocess pinned to one thread)
+# ---------------------------------------------------------------------------
+
+def oracle_single_page_sample(budget_s, max_steps=None):
+    """Oracle time of the single-page workload, extrapolated from a sample:
+    the full 288-row prefix prefill plus the first decode steps until
+    `budget_s` seconds (or max_steps) have elapsed."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    H, d, m, n, T = w.heads, w.head_dim, w.m, w.n, w.T
+    Q, K, V = workloads.qkv(m + T, H, d, 0, w.std, torch.bfloat16)
+    Q, K, V = (x.double().numpy() for x in (Q, K, V))
+    t0 = time.perf_counter()
+    oracle.prefill_attention(Q[:m], K[:m], V[:m], m, n)
+    state = oracle.prefill_cache(K[:m], V[:m], m, n, 0)
+    t1 = time.perf_counter()
+    steps = 0
+    while True:
+        state, _, _ = oracle.decode_step_fused(state, Q[m + steps], K[m + steps],
+                                               V[m + steps], n)
+        steps += 1
+        el = time.perf_counter() - t1
+        if el >= budget_s or steps >= T or (max_steps and steps >= max_steps):
+            break
+    t_pre, t_dec = t1 - t0, el / steps
+    est = t_pre + T * t_dec
+    return {"tokens_per_s": T / est, "prefill_s": t_pre, "decode_steps": steps,
+            "decode_s_per_step": t_dec}
+
+
+def run_cpu_worker(budget_s, max_steps=None):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker",
+           str(budget_s)]
+    if max_steps:
+        cmd += ["--cpu-max-steps", str(max_steps)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def main_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    for _ in range(args.warmup):
+        run_cpu_worker(0.5, max_steps=100)
+    vals, wall = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = run_cpu_worker(0.5, max_steps=100)
+        wall.append(time.perf_counter() - t0)
+        vals.append(r["tokens_per_s"])
+    v = statistics.mean(vals)
+    sample = ("oracle (CPU float64) on the single-page workload: the 288-row "
+              "prefix prefill plus the first 100 decode steps per timed step, "
+              "extrapolated to 6000 steps; one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(v, 2),
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * w.T / v, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "single_page_bf16", "batch": 1, "heads": 10,
+                   "head_dim": 128, "m": 288, "n": 128, "T": 6000},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample,
+                         "value": round(v, 2), "unit": "tokens/s"},
+        "e2e": {"value": round(v, 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main_ours(args):
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rswa.load()
+    peaks, peak_src = load_peaks()
+
+    # CPU baseline first (subprocess, one thread) on rank 0
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        cpu = run_cpu_worker(args.cpu_budget)
+
+    sp = setup_single_page(dev)
+    w = sp["w"]
+    s = sp["stream"]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        sp["g_prefill"].replay()
+        sp["g_decode"].replay()
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(s):
+            step()
+    torch.cuda.synchronize(dev)
+
+    # timed region: K steps, events per step, L2 flushed between steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            with torch.cuda.stream(s):
+                flush.zero_()
+            ev[i][0].record(s)
+            sp["g_prefill"].replay()
+            ev[i][1].record(s)
+            sp["g_decode"].replay()
+            ev[i][2].record(s)
+        torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    ms = statistics.mean(step_ms)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = t.item()
+    clocks = clk.summary()
+    cache_bytes = sp["cache"].cache_bytes(0)      # C(T) after the loop
+    tokens = w.batch * w.T * ws
+    value = tokens / (ms * 1e-3)
+
+    # dominant kernel: fused decode (6000 launches per step)
+    per_launch_ms = statistics.mean(dec_ms) / w.T
+    bpl = single_page_bytes_per_decode(w)
+    achieved = bpl / (per_launch_ms * 1e-3) / 1e9
+    roofline = {"kernel": "decode_kernel<bf16,128,fused>", "bound": "hbm",
+                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": recorded_traffic("decode_kernel"),
+                "peak_source": f"hbm_gbs ({peak_src})",
+                "algorithmic_bytes_per_launch": round(bpl),
+                "launch_us": round(per_launch_ms * 1e3, 3),
+                "note": ("launch duration = decode-graph time / 6000 (includes "
+                         "inter-launch gaps); the 2.1 MB working set stays in "
+                         "L2 across steps, so this batch-1 loop is latency-bound")}
+
+    # end-to-end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(sp, dev, args)
+
+    extras = None
+    if not args.no_extras and rank == 0:
+        del sp
+        torch.cuda.empty_cache()
+        extras = run_extras(dev, peaks, quick=args.quick)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "single_page_bf16", "batch": 1, "heads": 10,
+                       "head_dim": 128, "m": 288, "n": 128, "T": 6000,
+                       "parallelism": f"replicas x{ws}",
+                       "l2": "flushed (256 MB write) before every timed step",
+                       "graphs": "prefix prefill and 6000-step decode loop "
+                                 "replayed as two CUDA graphs"},
+            "roofline": roofline,
+            "cpu_baseline": None if cpu is None else {
+                "value": round(cpu["tokens_per_s"], 2), "unit": "tokens/s",
+                "cores": 1, "kind": "oracle",
+                "sample": ("full 288-row prefix prefill + first %d decode steps "
+                           "(%.1f ms/step) of the same workload, float64, one "
+                           "thread, extrapolated to 6000 steps"
+                           % (cpu["decode_steps"], 1e3 * cpu["decode_s_per_step"]))},
+            "e2e": e2e,
+            "gpu_launches": args.steps * (2 + w.T),
+            "clocks": clocks,
+            "cache_bytes_after_T": cache_bytes,
+            "extras": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(sp, dev, args):
+    """Same workload through the public API: per step the inputs are copied
+    from pinned host memory and the outputs read back, inside the timed
+    region."""
+    import torch
+    w = sp["w"]
+    s = sp["stream"]
+    hQ, hK, hV = (x.cpu().pin_memory() for x in (sp["Q"], sp["K"], sp["V"]))
+    hOp = torch.empty_like(sp["Op"], device="cpu").pin_memory()
+    hOd = torch.empty_like(sp["Od"], device="cpu").pin_memory()
+
+    def step():
+        with torch.cuda.stream(s):
+            sp["Q"].copy_(hQ, non_blocking=True)
+            sp["K"].copy_(hK, non_blocking=True)
+            sp["V"].copy_(hV, non_blocking=True)
+            sp["g_prefill"].replay()
+            sp["g_decode"].replay()
+            hOp.copy_(sp["Op"], non_blocking=True)
+            hOd.copy_(sp["Od"], non_blocking=True)
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        step()
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.mean(ts)
+    h2d = sum(x.numel() * x.element_size() for x in (hQ, hK, hV))
+    d2h = hOp.numel() * hOp.element_size() + hOd.numel() * hOd.element_size()
+    return {"value": round(w.batch * w.T / (ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms, 4)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-worker", type=float, default=None)
+    ap.add_argument("--cpu-max-steps", type=int, default=None)
+    args = ap.parse_args()
+    if args.cpu_worker is not None:
+        print(json.dumps(oracle_single_page_sample(args.cpu_worker,
+                                                   args.cpu_max_steps)))
+        return 0
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return main_reference(args)
+    return main_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

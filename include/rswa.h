@@ -1,0 +1,215 @@
+/*
+ * rswa.h - C ABI of the R-SWA (Reference Sliding Window Attention) library
+ * for GB300 (sm_103a).
+ *
+ * The method.  Every output token attends to the whole fixed reference prefix
+ * P of length m (visual tokens plus prompt, always visible) and to the last n
+ * output tokens, itself included (a causal sliding window; n = 128 by
+ * default).  The KV cache is therefore bounded: after T outputs it holds
+ * C(T) = m + min(n, T) <= m + n tokens, a queue of capacity m + n in which
+ * each new output evicts the oldest output, the (m+1)-th entry.
+ *   - "Unlimited-OCR deep dive" (ai-news-5min-kr): R-SWA pseudo-code block
+ *     N(t) = P U D_n(t) and C_R-SWA(T) = L_m + min(n, T); data-flow steps 2-4.
+ *   - "Unlimited OCR - Baidu's one-shot long-document parsing model"
+ *     (GeekNews): sections "Reference Sliding Window Attention (R-SWA)",
+ *     "KV cache management" and "Model architecture".
+ * Readings where the pages are silent: prefix rows attend causally among
+ * themselves; the window of n includes the current token; the softmax scale
+ * is 1/sqrt(head_dim); positions are applied by the caller (RoPE etc. before
+ * Q/K reach this library); one KV head per query head.
+ *
+ * Conventions shared by every call.
+ *   - All device pointers are plain CUDA device addresses owned by the
+ *     caller.  The library allocates no device memory: the cache lives in a
+ *     caller-provided buffer of rswa_cache_footprint() bytes.
+ *   - dtype is RSWA_F32 (float) or RSWA_BF16 (bfloat16) and applies to every
+ *     Q/K/V/O tensor of a cache; arithmetic is float32 in both cases.
+ *   - Token-major tensors: a "[rows][H][d]" tensor is contiguous with d
+ *     fastest.  Per-step tensors q, k, v, o are "[B][H][d]".
+ *   - Work is enqueued on the caller's stream (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) and returns immediately.
+ *     Arguments are validated on the host before anything is launched; an
+ *     invalid call launches nothing and changes no state.
+ *   - Every call returns an rswa_status.  RSWA_ECUDA reports a CUDA error
+ *     from a launch or copy; errors raised inside kernels (a bounded wait
+ *     that ran out) set a device flag that rswa_sync_status() returns.
+ *   - Calls on one cache must be ordered (same stream, or the caller orders
+ *     the streams); the cache state (m_b, t_b) is kept on the device and is
+ *     read and advanced by the kernels, so a captured CUDA graph replays
+ *     correctly.
+ */
+#ifndef RSWA_H
+#define RSWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RSWA_API __attribute__((visibility("default")))
+#else
+#define RSWA_API
+#endif
+
+/* Opaque host handle.  Holds the layout of the caller's device buffer. */
+typedef struct rswa_cache rswa_cache;
+
+enum rswa_status {
+  RSWA_OK = 0,
+  RSWA_EINVAL = 1,    /* bad argument: null pointer, size or shape */
+  RSWA_ECAPACITY = 2, /* a prefix longer than the cache's prefix capacity,
+                         or a buffer smaller than the footprint */
+  RSWA_EDTYPE = 3,    /* unsupported dtype / head_dim combination */
+  RSWA_EHANDLE = 4,   /* NULL, destroyed or foreign handle */
+  RSWA_ECUDA = 5,     /* a CUDA runtime call or launch failed */
+  RSWA_EDEVICE = 6    /* a kernel flagged an error (bounded wait ran out) */
+};
+
+enum rswa_dtype { RSWA_F32 = 0, RSWA_BF16 = 1 };
+
+/* Static message for a status code; never NULL. */
+RSWA_API const char* rswa_strerror(int status);
+
+/*
+ * Bytes of device memory a cache needs (written to *out_bytes).
+ *   m         prefix capacity per sequence (>= 0): the largest m_b a prefill
+ *             may store ("the prefix window m is fixed per inference",
+ *             GeekNews, R-SWA section).
+ *   n         output window (>= 1); the ring holds n output tokens.
+ *   heads     H >= 1, head_dim in {64, 128}, batch B >= 1.
+ * The footprint covers the prefix region K,V [B][H][m][d], the ring
+ * K,V [B][H][n][d], the per-sequence state (m_b, t_b) and the decode
+ * split-K scratch.  Errors: RSWA_EINVAL, RSWA_EDTYPE.
+ */
+RSWA_API int rswa_cache_footprint(int64_t m, int64_t n, int heads,
+                                  int head_dim, int batch, int dtype,
+                                  size_t* out_bytes);
+
+/*
+ * Create a cache over the caller's device buffer (>= footprint bytes,
+ * 256-byte aligned).  The buffer stays owned by the caller and must outlive
+ * the handle.  Creation zeroes the per-sequence state (every sequence empty:
+ * m_b = t_b = 0) with a synchronous memset on the current device.
+ * Errors: RSWA_EINVAL (null/misaligned buffer, bad sizes), RSWA_ECAPACITY
+ * (buffer too small), RSWA_EDTYPE, RSWA_ECUDA.
+ */
+RSWA_API int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim,
+                               int batch, int dtype, void* device_buf,
+                               size_t buf_bytes, rswa_cache** out);
+
+/* Free the host handle (not the device buffer).  Later use of the handle
+ * returns RSWA_EHANDLE. */
+RSWA_API int rswa_cache_destroy(rswa_cache* cache);
+
+/*
+ * Prefill: store every sequence's prefix and its last min(n, T) outputs in the
+ * cache, then (if O != NULL) compute R-SWA attention for every row.
+ *   Q, K, V   token-major packed rows [sum_b (m_b + T)][H][d]; sequence b
+ *             occupies rows off_b .. off_b + m_b + T - 1 with
+ *             off_b = sum_{b' < b} (m_b' + T).  Q may be NULL when O is NULL.
+ *   O         output rows, same layout as Q, or NULL (fill the cache only).
+ *   m_per_seq HOST array of B prefix lengths, 0 <= m_b <= m (capacity).
+ *   T         number of output rows per sequence already produced (>= 0).
+ * Row i of sequence b attends to keys j <= i with j < m_b (the prefix) or
+ * j > i - n (the window; "Unlimited-OCR deep dive", N(t) = P U D_n(t)).
+ * Cache effect: prefix rows 0..m_b-1 go to the static prefix region (encoded
+ * once, "no state transition", GeekNews, model architecture); output j goes
+ * to ring slot j mod n for j >= T - n; m_b and t_b = T are set.
+ * Inputs may contain no Inf/NaN: rows past a sequence's end are read but
+ * masked.  Errors: RSWA_EINVAL, RSWA_ECAPACITY (some m_b > m), RSWA_ECUDA.
+ */
+RSWA_API int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
+                          const void* V, void* O, const int64_t* m_per_seq,
+                          int64_t T, void* stream);
+
+/*
+ * Append output t_b's key and value for every sequence: k, v are [B][H][d].
+ * Writes ring slot t_b mod n - once t_b >= n this overwrites the oldest
+ * output, the (m+1)-th entry of the pages' queue (GeekNews, model
+ * architecture) - then advances t_b by one on the device.
+ * Errors: RSWA_EINVAL, RSWA_EHANDLE, RSWA_ECUDA.
+ */
+RSWA_API int rswa_append_kv(rswa_cache* cache, const void* k, const void* v,
+                            void* stream);
+
+/*
+ * One decode step: o = attention of q over the cache's m_b + min(n, t_b)
+ * keys for every (b, h).  q, o are [B][H][d]; lse (may be NULL) receives
+ * [B][H] float32 natural-log log-sum-exp of the scaled logits.  The caller
+ * appends token t's k, v before decoding q_t, so the token sees itself.
+ * Split-K over the prefix with a log-sum-exp combine inside the same launch;
+ * per-step cost depends on m_b + min(n, t_b) only, not on t_b (GeekNews,
+ * kernel analysis: constant decode-step duration under R-SWA).
+ * An empty cache yields o = 0 and lse = -inf.
+ * Errors: RSWA_EINVAL, RSWA_EHANDLE, RSWA_ECUDA.
+ */
+RSWA_API int rswa_decode_step(rswa_cache* cache, const void* q, void* o,
+                              float* lse, void* stream);
+
+/*
+ * rswa_append_kv(k, v) followed by rswa_decode_step(q) in one launch: the new
+ * key/value is attended straight from k, v and written to its ring slot by
+ * the same kernel; t_b advances once every head of the sequence is done.
+ * Same layouts and errors as the two calls it replaces.
+ */
+RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
+                                    const void* k, const void* v, void* o,
+                                    float* lse, void* stream);
+
+/*
+ * Live cache size of sequence b in bytes: C(t_b) * H * d * 2 (K and V) *
+ * element size, with C(t) = m_b + min(n, t) ("Unlimited-OCR deep dive",
+ * cache-size line; GeekNews, KV cache management).  Synchronous: waits for
+ * the device (cudaDeviceSynchronize) and reads m_b, t_b.  A test and
+ * reporting helper, not a hot-path call.  Errors: RSWA_EINVAL, RSWA_ECUDA.
+ */
+RSWA_API int rswa_cache_bytes(rswa_cache* cache, int b, size_t* out);
+
+/* Token count C(t_b) = m_b + min(n, t_b) of sequence b.  Synchronous like
+ * rswa_cache_bytes. */
+RSWA_API int rswa_cache_len(rswa_cache* cache, int b, int64_t* out);
+
+/* Number of outputs t_b appended so far to sequence b.  Synchronous. */
+RSWA_API int rswa_cache_get_t(rswa_cache* cache, int b, int64_t* out);
+
+/*
+ * Restore t_b for every sequence (t_per_seq: HOST array of B values >= 0),
+ * e.g. when resuming a saved cache.  The ring is taken to hold outputs
+ * t_b - min(n, t_b) .. t_b - 1 in slots j mod n; the call rewrites no
+ * key/value data.  Errors: RSWA_EINVAL, RSWA_ECUDA.
+ */
+RSWA_API int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq,
+                              void* stream);
+
+/*
+ * Byte offsets of the K and V slabs inside the cache buffer.  Each slab is
+ * [B][H][m + n][d] in the cache dtype: rows 0..m-1 of a (b, h) slab hold the
+ * prefix, rows m..m+n-1 the ring, output j in row m + (j mod n).  For
+ * inspection and checkpointing; host-only, no CUDA call.
+ * Errors: RSWA_EINVAL, RSWA_EHANDLE.
+ */
+RSWA_API int rswa_cache_kv_offsets(rswa_cache* cache, size_t* k_offset,
+                                   size_t* v_offset);
+
+/*
+ * Wait for all work on the current device, then report the first error a
+ * kernel flagged on this cache (RSWA_EDEVICE) or a CUDA error (RSWA_ECUDA),
+ * else RSWA_OK.  Clears the device flag.
+ */
+RSWA_API int rswa_sync_status(rswa_cache* cache);
+
+/*
+ * Host-side fault injection for tests: the next `count` calls that would
+ * touch CUDA fail with RSWA_ECUDA before launching anything.  No GPU fault is
+ * involved.
+ */
+RSWA_API void rswa_debug_fail_next_cuda(int count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSWA_H */

@@ -1,0 +1,387 @@
+// Host side of the C ABI: validation, cache layout, handle registry and
+// kernel dispatch.  No exception crosses the ABI; every entry point returns
+// an rswa_status.
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include "rswa_internal.h"
+
+using namespace rswa;
+
+struct rswa_cache {
+  CacheView cv;
+  int device;
+  void* buf;
+  size_t buf_bytes;
+};
+
+namespace {
+
+std::mutex g_mu;
+std::unordered_set<rswa_cache*> g_live;
+std::atomic<int> g_fail_next{0};
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool live(rswa_cache* c) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return c != nullptr && g_live.count(c) != 0;
+}
+
+// Test hook: simulated CUDA failure before anything is launched.
+bool injected_failure() {
+  int v = g_fail_next.load();
+  while (v > 0) {
+    if (g_fail_next.compare_exchange_weak(v, v - 1)) return true;
+  }
+  return false;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? RSWA_OK : RSWA_ECUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Makes the cache's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev)
+      cudaSetDevice(prev);
+  }
+};
+
+struct Layout {
+  size_t m_off, t_off, err_off, k_off, v_off, part_off, cnt_bh_off, cnt_b_off;
+  size_t total;
+  int chunk, max_chunks;
+};
+
+int valid_shape(int64_t m, int64_t n, int heads, int head_dim, int batch,
+                int dtype) {
+  if (dtype != RSWA_F32 && dtype != RSWA_BF16) return RSWA_EDTYPE;
+  if (head_dim != 64 && head_dim != 128) return RSWA_EDTYPE;
+  if (m < 0 || n < 1 || heads < 1 || batch < 1) return RSWA_EINVAL;
+  if (m > (int64_t(1) << 30) || n > (int64_t(1) << 30)) return RSWA_EINVAL;
+  if (heads > 4096 || batch > (1 << 20)) return RSWA_EINVAL;
+  return RSWA_OK;
+}
+
+// Keys per decode CTA: a power of two >= 64, chosen so that the largest
+// possible decode grid holds about 16 CTAs per SM of a 152-SM GB300.
+int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
+  const int64_t keys = (int64_t)batch * heads * (m + n);
+  const int64_t target = 152 * 16;
+  int64_t want = (keys + target - 1) / target;
+  int c = 64;
+  while (c < want && c < 2048) c <<= 1;
+  return c;
+}
+
+Layout make_layout(int64_t m, int64_t n, int heads, int head_dim, int batch,
+                   int dtype) {
+  Layout L{};
+  const size_t elt = dtype == RSWA_F32 ? 4 : 2;
+  L.chunk = choose_chunk(m, n, heads, batch);
+  L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
+  size_t off = 0;
+  L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);
+  L.t_off = off;      off = align_up(off + sizeof(int64_t) * batch);
+  L.err_off = off;    off = align_up(off + sizeof(int32_t));
+  L.cnt_bh_off = off; off = align_up(off + sizeof(int32_t) * batch * heads);
+  L.cnt_b_off = off;  off = align_up(off + sizeof(int32_t) * batch);
+  const size_t state_end = off;
+  (void)state_end;
+  L.k_off = off;
+  off = align_up(off + elt * (size_t)batch * heads * (size_t)(m + n) * head_dim);
+  L.v_off = off;
+  off = align_up(off + elt * (size_t)batch * heads * (size_t)(m + n) * head_dim);
+  L.part_off = off;
+  off = align_up(off + sizeof(float) * (size_t)batch * heads * L.max_chunks *
+                           (head_dim + 2));
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rswa_strerror(int status) {
+  switch (status) {
+    case RSWA_OK: return "ok";
+    case RSWA_EINVAL: return "invalid argument";
+    case RSWA_ECAPACITY: return "capacity exceeded (prefix longer than the cache's prefix capacity, or buffer too small)";
+    case RSWA_EDTYPE: return "unsupported dtype or head_dim";
+    case RSWA_EHANDLE: return "invalid or destroyed cache handle";
+    case RSWA_ECUDA: return "CUDA error";
+    case RSWA_EDEVICE: return "device-side error flagged by a kernel";
+    default: return "unknown status";
+  }
+}
+
+void rswa_debug_fail_next_cuda(int count) { g_fail_next.store(count < 0 ? 0 : count); }
+
+int rswa_cache_footprint(int64_t m, int64_t n, int heads, int head_dim,
+                         int batch, int dtype, size_t* out_bytes) {
+  if (!out_bytes) return RSWA_EINVAL;
+  const int st = valid_shape(m, n, heads, head_dim, batch, dtype);
+  if (st != RSWA_OK) return st;
+  *out_bytes = make_layout(m, n, heads, head_dim, batch, dtype).total;
+  return RSWA_OK;
+}
+
+int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim, int batch,
+                      int dtype, void* device_buf, size_t buf_bytes,
+                      rswa_cache** out) {
+  if (!out) return RSWA_EINVAL;
+  *out = nullptr;
+  const int st = valid_shape(m, n, heads, head_dim, batch, dtype);
+  if (st != RSWA_OK) return st;
+  if (!device_buf || (reinterpret_cast<uintptr_t>(device_buf) % kAlign) != 0)
+    return RSWA_EINVAL;
+  const Layout L = make_layout(m, n, heads, head_dim, batch, dtype);
+  if (buf_bytes < L.total) return RSWA_ECAPACITY;
+  if (injected_failure()) return RSWA_ECUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RSWA_ECUDA;
+
+  rswa_cache* c = new (std::nothrow) rswa_cache();
+  if (!c) return RSWA_ECUDA;
+  char* base = static_cast<char*>(device_buf);
+  CacheView& cv = c->cv;
+  cv.K = base + L.k_off;
+  cv.V = base + L.v_off;
+  cv.m_dev = reinterpret_cast<int32_t*>(base + L.m_off);
+  cv.t_dev = reinterpret_cast<int64_t*>(base + L.t_off);
+  cv.err = reinterpret_cast<int32_t*>(base + L.err_off);
+  cv.part = reinterpret_cast<float*>(base + L.part_off);
+  cv.cnt_bh = reinterpret_cast<int32_t*>(base + L.cnt_bh_off);
+  cv.cnt_b = reinterpret_cast<int32_t*>(base + L.cnt_b_off);
+  cv.B = batch;
+  cv.H = heads;
+  cv.d = head_dim;
+  cv.dtype = dtype;
+  cv.m_cap = m;
+  cv.n = n;
+  cv.slab_rows = m + n;
+  cv.chunk = L.chunk;
+  cv.max_chunks = L.max_chunks;
+  c->device = dev;
+  c->buf = device_buf;
+  c->buf_bytes = buf_bytes;
+  // Zero the state words (m_b, t_b, error flag, counters); K/V need no init.
+  cudaError_t e = cudaMemsetAsync(device_buf, 0, L.k_off, 0);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  if (e != cudaSuccess) {
+    delete c;
+    return RSWA_ECUDA;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_live.insert(c);
+  }
+  *out = c;
+  return RSWA_OK;
+}
+
+int rswa_cache_destroy(rswa_cache* cache) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!cache || g_live.erase(cache) == 0) return RSWA_EHANDLE;
+  }
+  delete cache;
+  return RSWA_OK;
+}
+
+int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
+                 const void* V, void* O, const int64_t* m_per_seq, int64_t T,
+                 void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  const CacheView& cv = cache->cv;
+  if (!K || !V || !m_per_seq || T < 0) return RSWA_EINVAL;
+  if (O && !Q) return RSWA_EINVAL;
+  if (!aligned16(K) || !aligned16(V) || (Q && !aligned16(Q)) ||
+      (O && !aligned16(O)))
+    return RSWA_EINVAL;
+  int64_t total_rows = 0;
+  for (int b = 0; b < cv.B; ++b) {
+    if (m_per_seq[b] < 0) return RSWA_EINVAL;
+    if (m_per_seq[b] > cv.m_cap) return RSWA_ECAPACITY;
+    total_rows += m_per_seq[b] + T;
+  }
+  if (T > (int64_t(1) << 40)) return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  int64_t row = 0;
+  for (int b0 = 0; b0 < cv.B; b0 += kMaxSeqPerLaunch) {
+    SeqTable st{};
+    st.seq0 = b0;
+    st.nseq = std::min(kMaxSeqPerLaunch, cv.B - b0);
+    st.T = T;
+    int64_t max_rows = 0, rows = 0;
+    int32_t tiles = 0;
+    st.tile_off[0] = 0;
+    for (int i = 0; i < st.nseq; ++i) {
+      const int64_t mb = m_per_seq[b0 + i];
+      st.m[i] = (int32_t)mb;
+      st.row_off[i] = row + rows;
+      rows += mb + T;
+      max_rows = std::max(max_rows, mb + std::min(cv.n, T));
+      tiles += (int32_t)((mb + T + 127) / 128);
+      st.tile_off[i + 1] = tiles;
+    }
+    cudaError_t e = launch_prefill_cache(cv, st, K, V, max_rows, s);
+    if (e != cudaSuccess) return RSWA_ECUDA;
+    if (O && rows > 0) {
+      if (prefill_tc_supported(cv))
+        e = launch_prefill_tc(cv, st, Q, K, V, O, rows, s);
+      else
+        e = launch_prefill_rowwise(cv, st, Q, K, V, O, rows, s);
+      if (e != cudaSuccess) return RSWA_ECUDA;
+    }
+    row += rows;
+  }
+  (void)total_rows;
+  return RSWA_OK;
+}
+
+int rswa_append_kv(rswa_cache* cache, const void* k, const void* v,
+                   void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  return status_of(launch_append(cache->cv, k, v, static_cast<cudaStream_t>(stream)));
+}
+
+int rswa_decode_step(rswa_cache* cache, const void* q, void* o, float* lse,
+                     void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!q || !o || !aligned16(q)) return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  return status_of(launch_decode(cache->cv, q, nullptr, nullptr, o, lse, false,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
+                           const void* v, void* o, float* lse, void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  return status_of(launch_decode(cache->cv, q, k, v, o, lse, true,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+static int read_state(rswa_cache* cache, int b, int64_t* m_b, int64_t* t_b) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (b < 0 || b >= cache->cv.B) return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  int32_t m32 = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return RSWA_ECUDA;
+  if (cudaMemcpy(&m32, cache->cv.m_dev + b, sizeof(m32), cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(t_b, cache->cv.t_dev + b, sizeof(*t_b), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+    return RSWA_ECUDA;
+  *m_b = m32;
+  return RSWA_OK;
+}
+
+int rswa_cache_len(rswa_cache* cache, int b, int64_t* out) {
+  if (!out) return RSWA_EINVAL;
+  int64_t m_b, t_b;
+  const int st = read_state(cache, b, &m_b, &t_b);
+  if (st != RSWA_OK) return st;
+  *out = m_b + std::min(cache->cv.n, t_b);
+  return RSWA_OK;
+}
+
+int rswa_cache_get_t(rswa_cache* cache, int b, int64_t* out) {
+  if (!out) return RSWA_EINVAL;
+  int64_t m_b, t_b;
+  const int st = read_state(cache, b, &m_b, &t_b);
+  if (st != RSWA_OK) return st;
+  *out = t_b;
+  return RSWA_OK;
+}
+
+int rswa_cache_bytes(rswa_cache* cache, int b, size_t* out) {
+  if (!out) return RSWA_EINVAL;
+  int64_t len = 0;
+  const int st = rswa_cache_len(cache, b, &len);
+  if (st != RSWA_OK) return st;
+  const size_t elt = cache->cv.dtype == RSWA_F32 ? 4 : 2;
+  *out = (size_t)len * cache->cv.H * cache->cv.d * 2 * elt;
+  return RSWA_OK;
+}
+
+int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq, void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!t_per_seq) return RSWA_EINVAL;
+  for (int b = 0; b < cache->cv.B; ++b)
+    if (t_per_seq[b] < 0) return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_set_t(cache->cv, t_per_seq, s) != cudaSuccess) return RSWA_ECUDA;
+  // The copy source is pageable host memory: finish before returning so the
+  // caller may release it.
+  return status_of(cudaStreamSynchronize(s));
+}
+
+int rswa_cache_kv_offsets(rswa_cache* cache, size_t* k_offset,
+                          size_t* v_offset) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!k_offset || !v_offset) return RSWA_EINVAL;
+  const char* base = static_cast<const char*>(cache->buf);
+  *k_offset = (size_t)(static_cast<const char*>(cache->cv.K) - base);
+  *v_offset = (size_t)(static_cast<const char*>(cache->cv.V) - base);
+  return RSWA_OK;
+}
+
+int rswa_sync_status(rswa_cache* cache) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return RSWA_ECUDA;
+  int32_t flag = 0;
+  if (cudaMemcpy(&flag, cache->cv.err, sizeof(flag), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return RSWA_ECUDA;
+  if (flag != 0) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(cache->cv.err, &zero, sizeof(zero), cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+      return RSWA_ECUDA;
+    return RSWA_EDEVICE;
+  }
+  return RSWA_OK;
+}
+
+}  // extern "C"

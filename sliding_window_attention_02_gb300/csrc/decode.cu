@@ -1,0 +1,169 @@
+// R-SWA decode step: split-K over the cache with a log-sum-exp combine.
+//
+// Grid (max_chunks, H, B).  The keys of sequence b are the prefix rows
+// 0..m_b-1 of its slab and the filled ring slots; CTA c of (b, h) takes
+// prefix chunk c (c < ceil(m_b / chunk)) or ring chunk c - ceil(m_b / chunk).
+// The number of CTAs per (b, h) depends on m_b only - never on t_b - so a
+// fused step may advance t_b while late CTAs of the same launch still start.
+//
+// Every CTA publishes (m, l, acc[d]) for its chunk; the last CTA of (b, h) to
+// arrive (atomic counter, no waiting) merges the partials and writes o and
+// lse.  Per-step cost is m_b + min(n, t_b) keys: flat in t_b once t_b >= n
+// ("Unlimited OCR", GeekNews, kernel analysis).
+#include "attend.cuh"
+
+namespace rswa {
+
+template <typename T, int D, bool FUSED>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
+              const T* __restrict__ vnew, T* __restrict__ o,
+              float* __restrict__ lse) {
+  using C = AttendCfg<T, D>;
+  constexpr int NW = kDecodeThreads / 32;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  const int64_t m_b = cv.m_dev[b];
+  const int chunk = cv.chunk;
+  const int cp = (int)((m_b + chunk - 1) / chunk);
+  const int cr = (int)((cv.n + chunk - 1) / chunk);
+  const int nch = cp + cr;
+  if (c >= nch) return;
+  const int64_t t_b = cv.t_dev[b];
+
+  const size_t bh = (size_t)b * cv.H + h;
+  const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
+  const T* kn = FUSED ? knew + bh * D : nullptr;
+  const T* vn = FUSED ? vnew + bh * D : nullptr;
+
+  int64_t j0, j1, sub = -1;
+  if (c < cp) {
+    j0 = (int64_t)c * chunk;
+    j1 = min(j0 + chunk, m_b);
+  } else {
+    const int64_t s0 = (int64_t)(c - cp) * chunk;
+    const int64_t filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
+    const int64_t s1 = max(s0, min(s0 + chunk, filled));
+    j0 = cv.m_cap + s0;
+    j1 = cv.m_cap + s1;
+    if (FUSED) {
+      const int64_t w = t_b % cv.n;  // slot of the new output
+      if (w >= s0 && w < s0 + chunk) {
+        sub = cv.m_cap + w;
+        // This CTA owns slot w: store the new k, v there.  No CTA of this
+        // launch reads slot w from the slab (it reads (knew, vnew) instead).
+        T* Kw = static_cast<T*>(cv.K) + (bh * cv.slab_rows + sub) * D;
+        T* Vw = static_cast<T*>(cv.V) + (bh * cv.slab_rows + sub) * D;
+        constexpr int NV = D * sizeof(T) / 16;
+        for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
+          if (i < NV)
+            reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(kn)[i];
+          else
+            reinterpret_cast<uint4*>(Vw)[i - NV] =
+                reinterpret_cast<const uint4*>(vn)[i - NV];
+        }
+      }
+    }
+  }
+
+  float qf[C::EPL];
+  load_q_frag<T, D>(q + bh * D, lane, qf);
+  SoftmaxState<C::EPL> st;
+  st.init();
+  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
+                     (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane, st);
+  merge_groups<T, D>(st);
+
+  // Merge the warps through shared memory.
+  __shared__ float s_m[NW], s_l[NW];
+  __shared__ float s_acc[NW][D];
+  if (lane < C::LPK) {
+#pragma unroll
+    for (int e = 0; e < C::EPL; ++e) s_acc[warp][lane * C::EPL + e] = st.acc[e];
+    if (lane == 0) {
+      s_m[warp] = st.m;
+      s_l[warp] = st.l;
+    }
+  }
+  __syncthreads();
+  const int tid = threadIdx.x;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
+  const float ref = (M == -INFINITY) ? 0.f : M;
+  float Ls = 0.f, A = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    const float sc = exp2f(s_m[w] - ref);
+    Ls += s_l[w] * sc;
+    if (tid < D) A += s_acc[w][tid] * sc;
+  }
+
+  // Publish this chunk's partial (m, l, acc[D]).
+  float* P = cv.part + (bh * cv.max_chunks) * (D + 2);
+  if (tid < D) P[c * (D + 2) + 2 + tid] = A;
+  if (tid == 0) {
+    P[c * (D + 2)] = M;
+    P[c * (D + 2) + 1] = Ls;
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) s_last = (atomicAdd(&cv.cnt_bh[bh], 1) == nch - 1);
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    float Mx = -INFINITY;
+    for (int k = 0; k < nch; ++k) Mx = fmaxf(Mx, __ldcg(P + k * (D + 2)));
+    const float r2 = (Mx == -INFINITY) ? 0.f : Mx;
+    float Lt = 0.f, At = 0.f;
+    for (int k = 0; k < nch; ++k) {
+      const float sc = exp2f(__ldcg(P + k * (D + 2)) - r2);
+      Lt += __ldcg(P + k * (D + 2) + 1) * sc;
+      if (tid < D) At += __ldcg(P + k * (D + 2) + 2 + tid) * sc;
+    }
+    if (tid < D) o[bh * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
+    if (tid == 0) {
+      if (lse) lse[bh] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;
+      cv.cnt_bh[bh] = 0;
+    }
+  }
+  if (FUSED && tid == 0) {
+    // The last CTA of sequence b (over all heads) advances t_b.  Every other
+    // CTA of b read t_b before its own arrival.
+    if (atomicAdd(&cv.cnt_b[b], 1) == cv.H * nch - 1) {
+      cv.cnt_b[b] = 0;
+      cv.t_dev[b] = t_b + 1;
+    }
+  }
+}
+
+template <typename T, int D>
+static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
+                                   const void* k, const void* v, void* o,
+                                   float* lse, bool fused, cudaStream_t s) {
+  dim3 grid(cv.max_chunks, cv.H, cv.B);
+  if (fused)
+    decode_kernel<T, D, true><<<grid, kDecodeThreads, 0, s>>>(
+        cv, (const T*)q, (const T*)k, (const T*)v, (T*)o, lse);
+  else
+    decode_kernel<T, D, false><<<grid, kDecodeThreads, 0, s>>>(
+        cv, (const T*)q, nullptr, nullptr, (T*)o, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
+                          const void* v, void* o, float* lse, bool fused,
+                          cudaStream_t s) {
+  if (cv.dtype == RSWA_F32) {
+    if (cv.d == 64) return launch_decode_t<float, 64>(cv, q, k, v, o, lse, fused, s);
+    return launch_decode_t<float, 128>(cv, q, k, v, o, lse, fused, s);
+  }
+  if (cv.d == 64)
+    return launch_decode_t<__nv_bfloat16, 64>(cv, q, k, v, o, lse, fused, s);
+  return launch_decode_t<__nv_bfloat16, 128>(cv, q, k, v, o, lse, fused, s);
+}
+
+}  // namespace rswa

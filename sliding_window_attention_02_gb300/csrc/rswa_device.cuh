@@ -1,0 +1,102 @@
+// Device helpers shared by the R-SWA kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "rswa_internal.h"
+
+namespace rswa {
+
+// log2(e): logits are pre-scaled by (1/sqrt(d)) * log2(e) so that the softmax
+// uses exp2.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device error codes written to CacheView::err (first one wins).
+enum DeviceErr : int32_t {
+  kErrNone = 0,
+  kErrWaitTimeout = 1,
+};
+
+__device__ __forceinline__ void flag_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// 16-byte streaming load through the read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Element traits: how many elements a 16-byte vector holds and how to widen.
+template <typename T>
+struct Elt;
+
+template <>
+struct Elt<float> {
+  static constexpr int kPerVec = 4;
+  __device__ __forceinline__ static void widen(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static uint4 narrow(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                      __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+
+template <>
+struct Elt<__nv_bfloat16> {
+  static constexpr int kPerVec = 8;
+  // bf16 -> f32 is exact: the bf16 bits are the top half of the f32 bits.
+  __device__ __forceinline__ static void widen(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  __device__ __forceinline__ static uint4 narrow(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// Running softmax state in log2 units: max m, sum l (relative to m) and the
+// weighted value accumulator acc (relative to m).
+template <int E>
+struct SoftmaxState {
+  float m, l;
+  float acc[E];
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  }
+  // Merge another state into this one.
+  __device__ __forceinline__ void merge(float m2, float l2, const float* a2) {
+    const float mn = fmaxf(m, m2);
+    const float ref = (mn == -INFINITY) ? 0.f : mn;
+    const float s1 = exp2f(m - ref);
+    const float s2 = exp2f(m2 - ref);
+    l = l * s1 + l2 * s2;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = acc[e] * s1 + a2[e] * s2;
+    m = mn;
+  }
+};
+
+}  // namespace rswa

@@ -1,0 +1,69 @@
+// Internal declarations shared by the host API and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rswa.h"
+
+namespace rswa {
+
+constexpr int kMaxSeqPerLaunch = 128;   // sequences per prefill launch
+constexpr int kDecodeThreads = 128;     // threads per decode CTA
+
+// Device view of a cache buffer.  All regions live in the caller's buffer.
+//   K, V    slabs [B][H][slab_rows][d], slab_rows = m_cap + n: rows
+//           0..m_cap-1 are the prefix region, rows m_cap..m_cap+n-1 the ring.
+//   m_dev   int32 [B]  prefix length m_b
+//   t_dev   int64 [B]  outputs appended t_b
+//   err     int32 [1]  first device-side error code (0 = none)
+//   part    float [B][H][max_chunks][d + 2]  split-K partials (m, l, acc)
+//   cnt_bh  int32 [B][H]  CTAs of (b, h) that have published a partial
+//   cnt_b   int32 [B]     CTAs of sequence b done (fused step: advances t_b)
+struct CacheView {
+  void* K;
+  void* V;
+  int32_t* m_dev;
+  int64_t* t_dev;
+  int32_t* err;
+  float* part;
+  int32_t* cnt_bh;
+  int32_t* cnt_b;
+  int B, H, d, dtype;
+  int64_t m_cap, n, slab_rows;
+  int chunk;       // keys per decode CTA
+  int max_chunks;  // ceil(m_cap / chunk) + ceil(n / chunk)
+};
+
+// Per-launch sequence table for prefill (passed by value as a kernel param).
+struct SeqTable {
+  int nseq;                              // sequences in this launch
+  int seq0;                              // index of the first one
+  int64_t T;                             // outputs per sequence
+  int64_t row_off[kMaxSeqPerLaunch];     // first row of each sequence
+  int32_t m[kMaxSeqPerLaunch];           // prefix lengths
+  int32_t tile_off[kMaxSeqPerLaunch + 1];// cumulative 128-row q-tiles
+};
+
+// ---- launchers (each returns the cudaError_t of its launch) ----
+cudaError_t launch_prefill_cache(const CacheView& cv, const SeqTable& st,
+                                 const void* K, const void* V, int64_t max_rows,
+                                 cudaStream_t s);
+cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
+                          cudaStream_t s);
+cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
+                         cudaStream_t s);
+cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
+                          const void* v, void* o, float* lse, bool fused,
+                          cudaStream_t s);
+cudaError_t launch_prefill_rowwise(const CacheView& cv, const SeqTable& st,
+                                   const void* Q, const void* K, const void* V,
+                                   void* O, int64_t total_rows, cudaStream_t s);
+// tcgen05 prefill (bf16, head_dim 128).  Returns cudaErrorNotSupported when
+// the shape is outside what the kernel handles.
+cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st,
+                              const void* Q, const void* K, const void* V,
+                              void* O, int64_t total_rows, cudaStream_t s);
+bool prefill_tc_supported(const CacheView& cv);
+
+}  // namespace rswa
