@@ -487,12 +487,13 @@ def main_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step():
-        sp["g_prefill"].replay()
-        sp["g_decode"].replay()
+        # CUDAGraph.replay() launches on the current stream
+        with torch.cuda.stream(s):
+            sp["g_prefill"].replay()
+            sp["g_decode"].replay()
 
     for _ in range(args.warmup):
-        with torch.cuda.stream(s):
-            step()
+        step()
     torch.cuda.synchronize(dev)
 
     # timed region: K steps, events per step, L2 flushed between steps
@@ -505,11 +506,11 @@ def main_ours(args):
         for i in range(args.steps):
             with torch.cuda.stream(s):
                 flush.zero_()
-            ev[i][0].record(s)
-            sp["g_prefill"].replay()
-            ev[i][1].record(s)
-            sp["g_decode"].replay()
-            ev[i][2].record(s)
+                ev[i][0].record(s)
+                sp["g_prefill"].replay()
+                ev[i][1].record(s)
+                sp["g_decode"].replay()
+                ev[i][2].record(s)
         torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()

@@ -211,18 +211,19 @@ int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
                  void* stream) {
   if (!live(cache)) return RSWA_EHANDLE;
   const CacheView& cv = cache->cv;
-  if (!K || !V || !m_per_seq || T < 0) return RSWA_EINVAL;
-  if (O && !Q) return RSWA_EINVAL;
-  if (!aligned16(K) || !aligned16(V) || (Q && !aligned16(Q)) ||
-      (O && !aligned16(O)))
-    return RSWA_EINVAL;
+  if (!m_per_seq || T < 0 || T > (int64_t(1) << 40)) return RSWA_EINVAL;
   int64_t total_rows = 0;
   for (int b = 0; b < cv.B; ++b) {
     if (m_per_seq[b] < 0) return RSWA_EINVAL;
     if (m_per_seq[b] > cv.m_cap) return RSWA_ECAPACITY;
     total_rows += m_per_seq[b] + T;
   }
-  if (T > (int64_t(1) << 40)) return RSWA_EINVAL;
+  // With no rows at all (every m_b = 0 and T = 0) the tensors may be NULL.
+  if (total_rows > 0 && (!K || !V)) return RSWA_EINVAL;
+  if (O && !Q) return RSWA_EINVAL;
+  if (!aligned16(K) || !aligned16(V) || (Q && !aligned16(Q)) ||
+      (O && !aligned16(O)))
+    return RSWA_EINVAL;
   if (injected_failure()) return RSWA_ECUDA;
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;

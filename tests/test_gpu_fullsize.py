@@ -34,6 +34,11 @@ def test_single_page_graph_replay(cuda_lib):
         sp["g_prefill"].replay()
         sp["g_decode"].replay()
     torch.cuda.synchronize()
+    # replay once more: every step restarts from an empty ring
+    with torch.cuda.stream(s):
+        sp["g_prefill"].replay()
+        sp["g_decode"].replay()
+    torch.cuda.synchronize()
     assert sp["cache"].sync_status() == 0
     Q, K, V = f64(sp["Q"]), f64(sp["K"]), f64(sp["V"])
     ts = [0, 1, 2, 126, 127, 128, 129, 255, 1000, 4097, T - 1]
