@@ -625,6 +625,56 @@ def measure_e2e(sp, dev, args):
             "ms_per_step": round(ms, 4)}
 
 
+def main_only(args):
+    """One workload, warmup + steps launches of its step, no timing lines
+    beyond a mean: the command the ncu summaries are taken from."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.Stream(device=dev)
+    if args.only == "single_page":
+        sp = setup_single_page(dev)
+        s = sp["stream"]
+
+        def step():
+            sp["g_prefill"].replay()
+            sp["g_decode"].replay()
+    elif args.only in ("batched", "sweep"):
+        st = setup_batched(dev) if args.only == "batched" else setup_sweep(dev)
+        w = st["w"]
+        if args.only == "sweep":
+            st["cache"].set_t([100000] * w.batch)
+        o = torch.empty(w.batch, w.heads, w.head_dim, dtype=torch.bfloat16,
+                        device=dev)
+        q, k, v = (x[:w.batch] for x in st["steps"])
+
+        def step():
+            st["cache"].decode_step_fused(q, k, v, o, stream=s)
+    else:
+        pf = setup_prefill(dev, layers=args.layers)
+        w = pf["w"]
+
+        def step():
+            for (Q, K, V), c, O in zip(pf["qkv"], pf["caches"], pf["outs"]):
+                c.prefill(Q, K, V, O, [w.m], w.T, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    ms = []
+    for _ in range(args.steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            step()
+            e1.record(s)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    print(json.dumps({"only": args.only, "ms_per_step": statistics.mean(ms)}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -638,6 +688,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--cpu-worker", type=float, default=None)
     ap.add_argument("--cpu-max-steps", type=int, default=None)
+    ap.add_argument("--only", default=None,
+                    choices=["single_page", "batched", "sweep", "prefill"],
+                    help="run one workload warmup+steps times and print its "
+                         "mean step time (for profiling)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="prefill layers with --only prefill")
     args = ap.parse_args()
     if args.cpu_worker is not None:
         print(json.dumps(oracle_single_page_sample(args.cpu_worker,
@@ -647,6 +703,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         return main_reference(args)
+    if args.only:
+        return main_only(args)
     return main_ours(args)
 
 
