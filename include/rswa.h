@@ -160,6 +160,39 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
                                     float* lse, void* stream);
 
 /*
+ * rswa_decode_step_fused without scratch from the cache buffer.  (Not part of
+ * the method on the pages: it has no counterpart there.)
+ *
+ * Who needs it: a caller whose device memory is fixed up front and who must
+ * not allocate once decoding runs - for example a serving loop that keeps a
+ * set budget of buffers, because cudaMalloc can stall the whole device while
+ * it synchronises and can fail when memory is fragmented, or a plug-in whose
+ * host application owns every device byte.  The split-K partials and arrival
+ * counters of this call live in a fixed 4 MiB array inside the library's own
+ * device memory (allocated when the library's device code is loaded and held
+ * by every GPU that loads it until the process exits).  The call itself
+ * allocates nothing and calls no allocating routine.
+ *
+ * Same arguments, layouts and result as rswa_decode_step_fused; the scratch
+ * region of the cache buffer goes unused by this call.
+ *   - Limit: the cache must need at most 4 MiB of scratch,
+ *     B * H * max_chunks * (d + 2) * 4 bytes of partials plus (B * H + B) * 4
+ *     bytes of counters, each rounded up to 256 bytes; a larger cache is
+ *     rejected with RSWA_ECAPACITY before anything runs.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current).  Make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents; each call clears its counters on the caller's stream first.
+ *     Calls that overlap on the GPU (other streams, other caches, other
+ *     threads) race on the array: order them.
+ * Errors: RSWA_EHANDLE, RSWA_EINVAL, RSWA_ECAPACITY, RSWA_ECUDA.
+ */
+RSWA_API int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
+                                           const void* k, const void* v,
+                                           void* o, float* lse, void* stream);
+
+/*
  * Live cache size of sequence b in bytes: C(t_b) * H * d * 2 (K and V) *
  * element size, with C(t) = m_b + min(n, t) ("Unlimited-OCR deep dive",
  * cache-size line; GeekNews, KV cache management).  Synchronous: waits for

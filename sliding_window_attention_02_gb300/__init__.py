@@ -20,7 +20,8 @@ __all__ = [
     "RSWA_F32", "RSWA_BF16",
     "rswa_strerror", "rswa_cache_footprint", "rswa_cache_create",
     "rswa_cache_destroy", "rswa_prefill", "rswa_append_kv",
-    "rswa_decode_step", "rswa_decode_step_fused", "rswa_cache_bytes",
+    "rswa_decode_step", "rswa_decode_step_fused",
+    "rswa_decode_step_fused_static", "rswa_cache_bytes",
     "rswa_cache_len", "rswa_cache_get_t", "rswa_cache_set_t",
     "rswa_sync_status", "rswa_debug_fail_next_cuda", "rswa_cache_kv_offsets",
     "RswaCache",
@@ -50,6 +51,8 @@ _SIGNATURES = {
     "rswa_decode_step": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
     "rswa_decode_step_fused": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                                         _c_vp, _c_vp]),
+    "rswa_decode_step_fused_static": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp,
+                                               _c_vp, _c_vp, _c_vp]),
     "rswa_cache_bytes": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_size)]),
     "rswa_cache_len": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_i64)]),
     "rswa_cache_get_t": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_i64)]),
@@ -174,6 +177,18 @@ def rswa_decode_step_fused(handle, q, k, v, o, lse=None, stream=None) -> None:
     _check(load().rswa_decode_step_fused(handle, _ptr(q), _ptr(k), _ptr(v),
                                          _ptr(o), _ptr(lse), _stream(stream)),
            "rswa_decode_step_fused")
+
+
+def rswa_decode_step_fused_static(handle, q, k, v, o, lse=None,
+                                  stream=None) -> None:
+    """rswa_decode_step_fused with its split-K scratch in the library's fixed
+    4 MiB device array instead of the cache buffer: the call allocates
+    nothing (for callers that must not allocate device memory once decoding
+    runs).  Overlapping calls race on that array."""
+    _check(load().rswa_decode_step_fused_static(handle, _ptr(q), _ptr(k),
+                                                _ptr(v), _ptr(o), _ptr(lse),
+                                                _stream(stream)),
+           "rswa_decode_step_fused_static")
 
 
 def rswa_cache_bytes(handle, b: int) -> int:

@@ -295,6 +295,24 @@ int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
                                  static_cast<cudaStream_t>(stream)));
 }
 
+int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
+                                  const void* k, const void* v, void* o,
+                                  float* lse, void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return RSWA_EINVAL;
+  size_t part_bytes = 0, cnt_bytes = 0;
+  if (static_scratch_need(cache->cv, &part_bytes, &cnt_bytes) >
+      static_scratch_capacity())
+    return RSWA_ECAPACITY;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  return status_of(launch_decode_fused_static(cache->cv, cache->device, q, k, v,
+                                              o, lse,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 static int read_state(rswa_cache* cache, int b, int64_t* m_b, int64_t* t_b) {
   if (!live(cache)) return RSWA_EHANDLE;
   if (b < 0 || b >= cache->cv.B) return RSWA_EINVAL;

@@ -66,4 +66,15 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st,
                               void* O, int64_t total_rows, cudaStream_t s);
 bool prefill_tc_supported(const CacheView& cv);
 
+// Fused decode step with split-K scratch in the library's static device array
+// (decode_static.cu).  Fails with cudaErrorInvalidValue when the cache needs
+// more than static_scratch_capacity() bytes of scratch.
+size_t static_scratch_need(const CacheView& cv, size_t* part_bytes,
+                           size_t* cnt_bytes);
+size_t static_scratch_capacity();
+cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
+                                       const void* q, const void* k,
+                                       const void* v, void* o, float* lse,
+                                       cudaStream_t s);
+
 }  // namespace rswa
