@@ -274,12 +274,36 @@ def events_time(fn, stream, iters, flush=None):
                 flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        fn()
-        e1.record(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
     return times
+
+
+GRAPH_STEPS = 16
+
+
+def graph_step_ms(step, stream, nsteps, iters):
+    """Mean ms per step: `nsteps` steps captured in one CUDA graph, replayed
+    `iters` times (after 2 warm-up replays), timed with events on `stream`.
+    Inputs of these workloads exceed L2, so no flush is needed."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(nsteps):
+            step()
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g.replay()
+    ts = events_time(lambda: g.replay(), stream, iters)
+    return statistics.mean(ts) / nsteps
 
 
 def run_extras(dev, peaks, quick=False):
@@ -299,11 +323,7 @@ def run_extras(dev, peaks, quick=False):
         idx[0] += 1
         bt["cache"].decode_step_fused(q[i * B:(i + 1) * B], k[i * B:(i + 1) * B],
                                       v[i * B:(i + 1) * B], o, stream=s)
-    with torch.cuda.stream(s):
-        for _ in range(5):
-            bstep()
-    ts = events_time(bstep, s, 10 if quick else 30)
-    ms = statistics.mean(ts)
+    ms = graph_step_ms(bstep, s, GRAPH_STEPS, 3 if quick else 10)
     nbytes = batched_step_bytes(bt["m_list"], w)
     gbs = nbytes / (ms * 1e-3) / 1e9
     out["batched_decode"] = {
@@ -311,7 +331,8 @@ def run_extras(dev, peaks, quick=False):
         "us_per_step": round(ms * 1e3, 2), "tokens_per_s": round(B / (ms * 1e-3), 1),
         "algorithmic_bytes": nbytes, "GB_per_s": round(gbs, 1),
         "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-        "l2": "inputs (%.2f GB) larger than L2" % (nbytes / 1e9)}
+        "l2": "inputs (%.2f GB) larger than L2" % (nbytes / 1e9),
+        "timing": "%d fused steps per CUDA graph, events around replays" % GRAPH_STEPS}
     del bt
     # decode sweep ----------------------------------------------------------
     sw = setup_sweep(dev)
@@ -330,11 +351,7 @@ def run_extras(dev, peaks, quick=False):
             idx[0] += 1
             sw["cache"].decode_step_fused(q[i * B:(i + 1) * B], k[i * B:(i + 1) * B],
                                           v[i * B:(i + 1) * B], o, stream=s)
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                sstep()
-        ts = events_time(sstep, s, 8 if quick else 20)
-        ms = statistics.mean(ts)
+        ms = graph_step_ms(sstep, s, GRAPH_STEPS, 3 if quick else 6)
         gbs = nbytes / (ms * 1e-3) / 1e9
         rows.append({"T": T, "us_per_step": round(ms * 1e3, 2),
                      "GB_per_s": round(gbs, 1),

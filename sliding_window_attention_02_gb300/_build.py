@@ -25,9 +25,10 @@ def _nvcc() -> str:
     return nv
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
+def _compile(src: str, verbose_ptxas: bool, defines=()) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [_nvcc(), *ARCH, *CFLAGS, "-I", CSRC, "-c", src, "-o", obj]
+    cmd = [_nvcc(), *ARCH, *CFLAGS, *[f"-D{d}" for d in defines], "-I", CSRC,
+           "-c", src, "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -38,12 +39,13 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    """Compile every translation unit in parallel and link librswa.so."""
+def build(verbose_ptxas: bool = False, defines=()) -> str:
+    """Compile every translation unit in parallel and link librswa.so.
+    `defines` are extra preprocessor definitions (tuning knobs)."""
     os.makedirs(BUILD, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, defines), srcs))
     tmp = LIB + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -55,4 +57,5 @@ def build(verbose_ptxas: bool = False) -> str:
 
 if __name__ == "__main__":
     import sys
-    print(build(verbose_ptxas="-v" in sys.argv))
+    defs = [a[2:] for a in sys.argv[1:] if a.startswith("-D")]
+    print(build(verbose_ptxas="-v" in sys.argv, defines=defs))

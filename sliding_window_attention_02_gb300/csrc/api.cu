@@ -79,11 +79,19 @@ int valid_shape(int64_t m, int64_t n, int heads, int head_dim, int batch,
   return RSWA_OK;
 }
 
+#ifndef RSWA_DECODE_CTAS_PER_SM
+#define RSWA_DECODE_CTAS_PER_SM 32
+#endif
+
 // Keys per decode CTA: a power of two >= 64, chosen so that the largest
-// possible decode grid holds about 16 CTAs per SM of a 152-SM GB300.
+// possible decode grid holds about RSWA_DECODE_CTAS_PER_SM CTAs per SM of a
+// 152-SM GB300.
 int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
+#ifdef RSWA_DECODE_CHUNK
+  return RSWA_DECODE_CHUNK;
+#endif
   const int64_t keys = (int64_t)batch * heads * (m + n);
-  const int64_t target = 152 * 16;
+  const int64_t target = 152 * RSWA_DECODE_CTAS_PER_SM;
   int64_t want = (keys + target - 1) / target;
   int c = 64;
   while (c < want && c < 2048) c <<= 1;

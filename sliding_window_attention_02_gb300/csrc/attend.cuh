@@ -12,12 +12,16 @@
 
 namespace rswa {
 
+#ifndef RSWA_DECODE_UNROLL
+#define RSWA_DECODE_UNROLL 8
+#endif
+
 template <typename T, int D>
 struct AttendCfg {
   static constexpr int EPL = Elt<T>::kPerVec;
   static constexpr int LPK = D / EPL;
   static constexpr int KPW = 32 / LPK;
-  static constexpr int U = 8;
+  static constexpr int U = RSWA_DECODE_UNROLL;
   static constexpr int KEYS_WARP = U * KPW;
   static_assert(D % EPL == 0 && 32 % LPK == 0, "unsupported head_dim");
 };
@@ -35,16 +39,19 @@ __device__ __forceinline__ void load_q_frag(const T* q_row, int lane,
   for (int e = 0; e < C::EPL; ++e) qf[e] *= sc;
 }
 
-// Attend rows [j_begin, j_end) of a key/value table whose row r starts at
-// Kb + r * stride (elements).  This warp takes the rows
-// j_begin + first + it * step + (0 .. KEYS_WARP-1).  A row equal to sub_row
-// is read from (knew, vnew) instead of the table.
+// Attend logical rows [j_begin, j_end) of a key/value table whose physical
+// row p starts at Kb + p * stride (elements); logical row r maps to
+// p = r for r < seg_end and p = r + gap beyond it (two segments of one
+// table, e.g. the prefix rows and the ring slots of a cache slab).  This warp
+// takes the rows j_begin + first + it * step + (0 .. KEYS_WARP-1).  A row
+// whose physical index equals sub_row is read from (knew, vnew) instead.
 template <typename T, int D>
 __device__ __forceinline__ void attend_range(
     const float* qf, const T* __restrict__ Kb, const T* __restrict__ Vb,
     int64_t stride, int64_t j_begin, int64_t j_end, int64_t first,
     int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
-    SoftmaxState<AttendCfg<T, D>::EPL>& st) {
+    SoftmaxState<AttendCfg<T, D>::EPL>& st, int64_t seg_end = INT64_MAX,
+    int64_t gap = 0) {
   using C = AttendCfg<T, D>;
   constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
   const int grp = lane / LPK;
@@ -56,7 +63,8 @@ __device__ __forceinline__ void attend_range(
     for (int u = 0; u < U; ++u) {
       const int64_t row = base + u * KPW + grp;
       ok[u] = row < j_end;
-      const int64_t r = ok[u] ? row : j_begin;
+      const int64_t lr = ok[u] ? row : j_begin;
+      const int64_t r = lr < seg_end ? lr : lr + gap;
       const T* kp = Kb + r * stride + col;
       const T* vp = Vb + r * stride + col;
       if (r == sub_row) {

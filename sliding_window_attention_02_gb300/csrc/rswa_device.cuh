@@ -23,6 +23,16 @@ __device__ __forceinline__ void flag_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch: wait for the preceding grid of the stream
+// (a no-op when the kernel was not launched as a dependent), and allow the
+// next grid to begin launching.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 16-byte streaming load through the read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
