@@ -1,25 +1,31 @@
 // R-SWA prefill on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// One CTA computes one 128-row query tile of one head:
+// Computes, for every row i of every sequence and head,
 //   O_i = softmax_{j in N(i)}(q_i . k_j / sqrt(d)) . v_j,
 //   N(i) = {j <= i}                                   for prefix rows i < m,
 //   N(i) = {j < m} U {j : max(m, i - n + 1) <= j <= i} for output rows,
 // ("Unlimited-OCR deep dive": N(t) = P U D_n(t); "Unlimited OCR", GeekNews:
-// the two-segment window of size m + n).  Key tiles of 128 rows are visited
-// only if the mask admits at least one (row, key) pair of the tile: the
-// prefix tiles 0 .. ceil(m/128)-1 up to the diagonal, plus the band tiles
-// that hold the last n keys of the tile's output rows.  Per-element masking
-// runs only on tiles the mask covers partially.
+// the two-segment window of size m + n).
 //
-// Warp roles (256 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles into a 2-stage ring
-//   warp 1      TMEM allocator and MMA issuer (one thread):
-//                 S_j = Q K_j^T   -> TMEM (two S buffers, ping-pong)
-//                 O  += P_j V_j   -> TMEM
-//   warps 4..7  softmax: thread r owns query row r (= TMEM lane r); reads
-//               S_j from TMEM, masks, exponentiates, writes P_j (bf16) to
-//               shared memory, rescales O in TMEM when its running maximum
-//               grows by more than 2^8, and finally normalises O.
+// One CTA owns two adjacent 128-row query tiles ("halves") of one head and
+// walks the union of their key tiles: the prefix tiles 0 .. ceil(m/128)-1 up
+// to the diagonal, then the band tiles that hold the last n keys of the
+// output rows.  Tiles the mask excludes entirely are never loaded.  Both
+// halves share every K and V tile.  Per-element masking runs only on tiles
+// the mask covers partially for that half.
+//
+// Roles (320 threads):
+//   warps 0-3   softmax of half 0 (thread r owns row r = TMEM lane r)
+//   warps 4-7   softmax of half 1
+//   warp 8      TMA producer: Q0, Q1, then K_j, V_j into a 4-slot ring
+//   warp 9      TMEM allocator and MMA issuer (one thread)
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_h (bf16,
+// two per column) overwrites the first 64 columns of S_h once S_h is read,
+// and feeds the PV MMA straight from TMEM.  The issue order
+//   QK0(0) QK1(0) | PV0(j) QK0(j+1) PV1(j) QK1(j+1) | ...
+// keeps the tensor core on one half while the other half's softmax runs, and
+// relies on the in-order execution of one thread's tcgen05.mma stream for
+// S_h being rewritten only after PV_h has read P_h.
 // Every wait is bounded; on a timeout the CTA drains its own copies and MMAs,
 // frees TMEM, sets the cache's device error flag and exits.
 #include <cuda.h>
@@ -32,24 +38,35 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = 128;                       // query rows per CTA
-constexpr int BN = 128;                       // keys per tile
-constexpr int HD = 128;                       // head_dim
-constexpr int kThreads = 256;
-constexpr uint32_t kSub = BM * 64 * 2;        // [128][64] bf16, 128B-swizzled
-constexpr uint32_t kTileB = 2 * kSub;         // [128][128] bf16
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + kTileB;    // 2 stages
-constexpr uint32_t OFF_V = OFF_K + 2 * kTileB;// 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * kTileB;
-constexpr uint32_t OFF_BAR = OFF_P + kTileB;
+constexpr int BM = 128;                        // rows per half
+constexpr int BN = 128;                        // keys per tile
+constexpr int HD = 128;                        // head_dim
+constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int NS = 4;                          // K/V ring slots
+constexpr uint32_t kSub = BM * 64 * 2;         // [128][64] bf16, 128B-swizzled
+constexpr uint32_t kTileB = 2 * kSub;          // [128][128] bf16 = 32 KB
+constexpr uint32_t OFF_Q = 0;                  // Q0, Q1
+constexpr uint32_t OFF_RING = 2 * kTileB;
+constexpr uint32_t OFF_BAR = OFF_RING + NS * kTileB;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + 1 KB alignment slack
 
-constexpr uint32_t TM_O = 0, TM_S0 = 128, TM_S1 = 256, TM_COLS = 512;
-constexpr float kRescaleThreshold = 8.0f;     // log2 units
+__host__ __device__ constexpr uint32_t tm_s(int half) { return half ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t tm_o(int half) { return half ? 384u : 256u; }
+constexpr uint32_t TM_COLS = 512;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-enum Bar { B_Q, B_KF0, B_KF1, B_VF0, B_VF1, B_E0, B_E1, B_S0, B_S1, B_P, B_O, B_FIN, NBAR };
+// barrier indices
+constexpr int B_Q = 0;
+constexpr int B_FULL = 1;                      // NS slots
+constexpr int B_EMPTY = B_FULL + NS;           // NS slots
+constexpr int B_S = B_EMPTY + NS;              // 2 halves
+constexpr int B_P = B_S + 2;                   // 2 halves
+constexpr int B_O = B_P + 2;                   // 2 halves
+constexpr int B_FIN = B_O + 2;
+constexpr int NBAR = B_FIN + 1;
 
 struct TileRange {
   int np;        // prefix tiles 0 .. np-1
@@ -57,28 +74,42 @@ struct TileRange {
   int nt;        // tiles visited
 };
 
-__device__ __forceinline__ TileRange tile_range(int qt, int m, int n, int L) {
-  TileRange r;
-  const int q0 = qt * BM;
-  const int i_hi = min(q0 + BM - 1, L - 1);
-  r.np = min((m + BN - 1) / BN, qt + 1);
-  const int i_lo = max(q0, m);
+// Key tiles visited by rows [r_lo, r_hi] of a sequence with prefix m,
+// window n and length L.
+__device__ __forceinline__ TileRange tile_range(int r_lo, int r_hi, int m, int n,
+                                                int L) {
+  TileRange t;
+  const int i_hi = min(r_hi, L - 1);
+  t.np = min((m + BN - 1) / BN, i_hi / BN + 1);
+  const int i_lo = max(r_lo, m);
   int nb = 0;
-  r.kb_start = r.np;
+  t.kb_start = t.np;
   if (i_lo <= i_hi) {
     const int band_lo = max(m, i_lo - n + 1);
-    r.kb_start = max(band_lo / BN, r.np);
-    nb = max(0, i_hi / BN - r.kb_start + 1);
+    t.kb_start = max(band_lo / BN, t.np);
+    nb = max(0, i_hi / BN - t.kb_start + 1);
   }
-  r.nt = r.np + nb;
-  return r;
+  t.nt = t.np + nb;
+  return t;
 }
 
-__device__ __forceinline__ int tile_at(const TileRange& r, int j) {
-  return j < r.np ? j : r.kb_start + (j - r.np);
+__device__ __forceinline__ int tile_at(const TileRange& t, int j) {
+  return j < t.np ? j : t.kb_start + (j - t.np);
 }
 
-// 32 TMEM columns of this warp's 32 lanes, completed before returning.
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16, f32 accumulate).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                            uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 columns of this warp's 32 lanes, completed before returning.
 __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -95,12 +126,38 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t* r) {
+// 128 columns in four loads and one wait.  The empty asm statements after
+// the wait re-define the registers so no use can move above the wait.
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t* r) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t* q = r + 32 * c;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]),
+          "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
+          "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]),
+          "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]),
+          "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]), "=r"(q[26]),
+          "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
+        : "r"(taddr + 32 * c)
+        : "memory");
+  }
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int c = 0; c < 128; c += 8)
+    asm volatile(""
+                 : "+r"(r[c]), "+r"(r[c + 1]), "+r"(r[c + 2]), "+r"(r[c + 3]),
+                   "+r"(r[c + 4]), "+r"(r[c + 5]), "+r"(r[c + 6]), "+r"(r[c + 7]));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
       "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
       "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
@@ -119,38 +176,41 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, CacheView cv,
-                  SeqTable st, __nv_bfloat16* __restrict__ O, int total_tiles) {
+                  SeqTable st, __nv_bfloat16* __restrict__ O, int total_pairs) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar0 = sb + OFF_BAR;
-  auto bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto bar = [&](int k) { return bar0 + 8u * (uint32_t)k; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 8 * NBAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * NBAR + 4);
+  volatile int* abort_flag =
+      reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * NBAR + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + OFF_BAR + 8 * NBAR + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = cv.H;
   const int h = blockIdx.x % H;
-  const int g = total_tiles - 1 - (int)(blockIdx.x / H);  // heavy tiles first
+  const int g = total_pairs - 1 - (int)(blockIdx.x / H);  // heavy pairs first
   int sl = 0;
   while (sl + 1 < st.nseq && st.tile_off[sl + 1] <= g) ++sl;
-  const int qt = g - st.tile_off[sl];
+  const int pr = g - st.tile_off[sl];                      // pair in sequence
   const int m = st.m[sl];
   const int n = (int)min(cv.n, (int64_t)1 << 30);
   const int L = m + (int)st.T;
   const int64_t row0 = st.row_off[sl];
-  const TileRange tr = tile_range(qt, m, n, L);
+  const int q0 = pr * 2 * BM;
+  const TileRange tr = tile_range(q0, q0 + 2 * BM - 1, m, n, L);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(bar(i), i == B_P ? 128u : 1u);
+    for (int k = 0; k < NBAR; ++k)
+      mbar_init(bar(k), (k == B_P || k == B_P + 1) ? 128u : 1u);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
   }
@@ -159,125 +219,162 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const int x0 = h * HD;
-      const int yq = (int)(row0 + (int64_t)qt * BM);
-      mbar_arrive_expect_tx(bar(B_Q), kTileB);
+      const int yq = (int)(row0 + q0);
+      mbar_arrive_expect_tx(bar(B_Q), 2 * kTileB);
       tma_load_2d(sb + OFF_Q, &tmQ, x0, yq, bar(B_Q));
       tma_load_2d(sb + OFF_Q + kSub, &tmQ, x0 + 64, yq, bar(B_Q));
+      tma_load_2d(sb + OFF_Q + kTileB, &tmQ, x0, yq + BM, bar(B_Q));
+      tma_load_2d(sb + OFF_Q + kTileB + kSub, &tmQ, x0 + 64, yq + BM, bar(B_Q));
       int issued = 0;
-      for (int j = 0; j < tr.nt; ++j) {
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar(B_E0 + s), ((j >> 1) - 1) & 1, abort_flag,
-                                 kWaitLimitNs))
+      for (int idx = 0; idx < 2 * tr.nt; ++idx) {
+        const int s = idx % NS;
+        if (idx >= NS && !mbar_wait(bar(B_EMPTY + s), ((idx / NS) - 1) & 1,
+                                    abort_flag, kWaitLimitNs))
           break;
-        const int y = (int)(row0 + (int64_t)tile_at(tr, j) * BN);
-        mbar_arrive_expect_tx(bar(B_KF0 + s), kTileB);
-        tma_load_2d(sb + OFF_K + s * kTileB, &tmK, x0, y, bar(B_KF0 + s));
-        tma_load_2d(sb + OFF_K + s * kTileB + kSub, &tmK, x0 + 64, y, bar(B_KF0 + s));
-        mbar_arrive_expect_tx(bar(B_VF0 + s), kTileB);
-        tma_load_2d(sb + OFF_V + s * kTileB, &tmV, x0, y, bar(B_VF0 + s));
-        tma_load_2d(sb + OFF_V + s * kTileB + kSub, &tmV, x0 + 64, y, bar(B_VF0 + s));
+        const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
+        const int y = (int)(row0 + (int64_t)tile_at(tr, idx >> 1) * BN);
+        const uint32_t dst = sb + OFF_RING + s * kTileB;
+        mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
+        tma_load_2d(dst, map, x0, y, bar(B_FULL + s));
+        tma_load_2d(dst + kSub, map, x0 + 64, y, bar(B_FULL + s));
         ++issued;
       }
       // Drain: every copy issued has landed before the CTA may exit.
       mbar_wait(bar(B_Q), 0, never, kWaitLimitNs);
-      for (int j = max(0, issued - 2); j < issued; ++j) {
-        mbar_wait(bar(B_KF0 + (j & 1)), (j >> 1) & 1, never, kWaitLimitNs);
-        mbar_wait(bar(B_VF0 + (j & 1)), (j >> 1) & 1, never, kWaitLimitNs);
-      }
+      for (int idx = max(0, issued - NS); idx < issued; ++idx)
+        mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, never, kWaitLimitNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, HD, true);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j & 1;
-        if (!mbar_wait(bar(B_KF0 + s), (j >> 1) & 1, abort_flag, kWaitLimitNs))
-          return false;
-        tc_fence_after();
-        const uint32_t d = tmem + (s ? TM_S1 : TM_S0);
+      auto wait_slot = [&](int idx) {
+        return mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, abort_flag,
+                         kWaitLimitNs);
+      };
+      // S_h = Q_h K^T from the K tile in ring slot of load idx.
+      auto qk = [&](int half, int idx) {
+        const uint32_t kb = sb + OFF_RING + (idx % NS) * kTileB;
+        const uint32_t qb = sb + OFF_Q + half * kTileB;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
-          mma_bf16_ss(d, desc_sw128(sb + OFF_Q + off, 16, 1024),
-                      desc_sw128(sb + OFF_K + s * kTileB + off, 16, 1024), idesc_qk,
-                      k > 0);
+          mma_bf16_ss(tmem + tm_s(half), desc_sw128(qb + off, 16, 1024),
+                      desc_sw128(kb + off, 16, 1024), idesc_qk, k > 0);
         }
-        mma_commit(bar(B_S0 + s));
-        return true;
+        mma_commit(bar(B_S + half));
       };
-      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, kWaitLimitNs);
-      if (ok) tc_fence_after();
-      if (ok && tr.nt > 0) ok = issue_qk(0);
-      for (int j = 0; ok && j < tr.nt; ++j) {
-        if (j + 1 < tr.nt && !issue_qk(j + 1)) break;
-        const int s = j & 1;
-        if (!mbar_wait(bar(B_P), j & 1, abort_flag, kWaitLimitNs)) break;
-        if (!mbar_wait(bar(B_VF0 + s), (j >> 1) & 1, abort_flag, kWaitLimitNs)) break;
-        tc_fence_after();
+      // O_h (+)= P_h V from TMEM P_h and the V tile of load idx.
+      auto pv = [&](int half, int idx, bool acc) {
+        const uint32_t vb = sb + OFF_RING + (idx % NS) * kTileB;
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * kSub + (k & 3) * 32;
-          mma_bf16_ss(tmem + TM_O, desc_sw128(sb + OFF_P + aoff, 16, 1024),
-                      desc_sw128(sb + OFF_V + s * kTileB + k * 2048, kSub, 1024),
-                      idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < BN / 16; ++k)
+          mma_bf16_ts(tmem + tm_o(half), tmem + tm_s(half) + k * 8,
+                      desc_sw128(vb + k * 2048, kSub, 1024), idesc_pv,
+                      (acc || k > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, kWaitLimitNs) && tr.nt > 0;
+      if (ok) {
+        tc_fence_after();
+        ok = wait_slot(0);
+        if (ok) {
+          tc_fence_after();
+          qk(0, 0);
+          qk(1, 0);
+          mma_commit(bar(B_EMPTY + 0));
         }
-        mma_commit(bar(B_O));
-        mma_commit(bar(B_E0 + s));
+      }
+      for (int j = 0; ok && j < tr.nt; ++j) {
+        const int vi = 2 * j + 1, ki = 2 * j + 2;
+        const bool more = j + 1 < tr.nt;
+        if (!mbar_wait(bar(B_P + 0), j & 1, abort_flag, kWaitLimitNs) || !wait_slot(vi))
+          break;
+        tc_fence_after();
+        pv(0, vi, j > 0);
+        if (more) {
+          if (!wait_slot(ki)) break;
+          tc_fence_after();
+          qk(0, ki);
+        } else {
+          mma_commit(bar(B_O + 0));
+        }
+        if (!mbar_wait(bar(B_P + 1), j & 1, abort_flag, kWaitLimitNs)) break;
+        tc_fence_after();
+        pv(1, vi, j > 0);
+        mma_commit(bar(B_EMPTY + vi % NS));
+        if (more) {
+          qk(1, ki);
+          mma_commit(bar(B_EMPTY + ki % NS));
+        } else {
+          mma_commit(bar(B_O + 1));
+        }
       }
       // Drain: all MMAs of this CTA have finished before TMEM is freed.
       mma_commit(bar(B_FIN));
       mbar_wait(bar(B_FIN), 0, never, kWaitLimitNs);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int r = threadIdx.x - 128;                     // row in tile
+    const int half = warp >> 2;
+    const int r = threadIdx.x & 127;                    // row in half
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int i = qt * BM + r;                           // row in sequence
+    const int qh = q0 + half * BM;                      // first row of half
+    const int i = qh + r;                               // row in sequence
     const float sl2 = rsqrtf((float)HD) * kLog2e;
+    const uint32_t s_addr = tmem + lane_off + tm_s(half);
+    const uint32_t o_addr = tmem + lane_off + tm_o(half);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < tr.nt; ++j) {
-      const int s = j & 1;
       const int k0 = tile_at(tr, j) * BN;
-      const int q0 = qt * BM;
-      // Tile fully visible: every key <= every row, and every key either in
-      // the prefix or inside every row's window.
-      const bool full = (k0 + BN - 1 <= q0) &&
-                        ((k0 + BN - 1 < m) || (max(k0, m) > q0 + BM - 1 - n));
-      if (!mbar_wait(bar(B_S0 + s), (j >> 1) & 1, abort_flag, kWaitLimitNs)) {
+      // Tile fully visible for this half: every key <= every row, and every
+      // key either in the prefix or inside every row's window.
+      const bool full = (k0 + BN - 1 <= qh) &&
+                        ((k0 + BN - 1 < m) || (max(k0, m) > qh + BM - 1 - n));
+      if (!mbar_wait(bar(B_S + half), j & 1, abort_flag, kWaitLimitNs)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // Pass 1: row maximum of the visible logits (raw q.k; the positive
-      // scale is applied afterwards).
-      const uint32_t sa = tmem + lane_off + (s ? TM_S1 : TM_S0);
-      const int hi = i - k0;          // visible: c <= hi && (c < a || c > b)
+      // Pass 1: row maximum over the visible logits, 32 columns at a time.
+      const int hi = i - k0;   // visible: c <= hi && (c < a || c > b)
       const int a = m - k0;
       const int b = i - n - k0;
-      float tmax = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32_sync(sa + c * 32, v);
+        tmem_ld32_sync(s_addr + c0, v);
+        if (!full) {
+          // Mask in place and write back, so pass 2 reads masked logits.
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          const bool vis = full || (col <= hi && (col < a || col > b));
-          tmax = fmaxf(tmax, vis ? __uint_as_float(v[e]) : -INFINITY);
+          for (int e = 0; e < 32; ++e) {
+            const int c = c0 + e;
+            if (!(c <= hi && (c < a || c > b))) v[e] = 0xff800000u;  // -inf
+          }
+          tmem_st32(s_addr + c0, v);
+        }
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          mx[0] = fmaxf(mx[0], __uint_as_float(v[e]));
+          mx[1] = fmaxf(mx[1], __uint_as_float(v[e + 1]));
+          mx[2] = fmaxf(mx[2], __uint_as_float(v[e + 2]));
+          mx[3] = fmaxf(mx[3], __uint_as_float(v[e + 3]));
         }
       }
-      tmax *= sl2;
+      if (!full) tmem_wait_st();
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
       // Lazy rescale: keep the reference maximum unless it grew by > 2^8.
-      // Exact either way: O and l share the reference.
+      // Exact either way: O and l share the reference.  O_h is stable here:
+      // S_h(j) completing implies PV_h(j-1) completed (one MMA stream).
       float alpha = 1.f;
       bool resc = false;
       const float m_new = fmaxf(m_run, tmax);
@@ -289,67 +386,53 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         l_run *= alpha;
         resc = true;
       }
-      const float ref = (m_run == -INFINITY) ? 0.f : m_run;
-      // PV of the previous tile must be done: P buffer free, O stable.
-      if (j > 0 && !mbar_wait(bar(B_O), (j - 1) & 1, abort_flag, kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
-          const uint32_t oa = tmem + lane_off + TM_O + c * 32;
-          tmem_ld32_sync(oa, o);
+          tmem_ld32_sync(o_addr + c * 32, o);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32_sync(oa, o);
+          tmem_st32(o_addr + c * 32, o);
         }
       }
-      // Pass 2: P = exp2(x - ref) -> bf16 -> shared memory, 128B-swizzled
-      // K-major as the MMA reads it, in 16-byte chunks of 8 keys.
-      uint8_t* prow = smem + OFF_P + (r >> 3) * 1024 + (r & 7) * 128;
-      float psum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32_sync(sa + c * 32, v);
-        uint32_t w[16];
+      // Pass 2: P_h = exp2(x - ref) as bf16 -> TMEM over the first 64
+      // columns of S_h (two bf16 per column), 64 logits at a time.  Columns
+      // 0..63 of S_h are read before any P column is written.
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[2][32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = c * 32 + 2 * e;
-          const bool v0 = full || (c0 <= hi && (c0 < a || c0 > b));
-          const bool v1 = full || (c0 + 1 <= hi && (c0 + 1 < a || c0 + 1 > b));
-          const float p0 = v0 ? ex2(fmaf(__uint_as_float(v[2 * e]), sl2, -ref)) : 0.f;
-          const float p1 = v1 ? ex2(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -ref)) : 0.f;
-          psum += p0 + p1;
-          w[e] = pack_bf16(p0, p1);
-        }
+      for (int hc = 0; hc < 2; ++hc) {
+        uint32_t v[64];
+        tmem_ld32_sync(s_addr + 64 * hc, v);
+        tmem_ld32_sync(s_addr + 64 * hc + 32, v + 32);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c16 = c * 4 + q;
-          uint8_t* dst = prow + (c16 >> 3) * kSub + (((c16 & 7) ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        for (int c = 0; c < 32; ++c) {
+          const int e = 2 * c;
+          const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, nref));
+          const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, nref));
+          ps[c & 3] += p0 + p1;
+          pk[hc][c] = pack_bf16(p0, p1);
         }
       }
-      l_run += psum;
-      fence_proxy_async_smem();
+      tmem_st32(s_addr, pk[0]);
+      tmem_st32(s_addr + 32, pk[1]);
+      l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(B_P));
+      mbar_arrive(bar(B_P + half));
     }
     // Epilogue: O / l -> bf16 -> global.
-    if (ok && tr.nt > 0 &&
-        mbar_wait(bar(B_O), (tr.nt - 1) & 1, abort_flag, kWaitLimitNs)) {
+    if (ok && tr.nt > 0 && mbar_wait(bar(B_O + half), 0, abort_flag, kWaitLimitNs)) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16* orow = O + ((row0 + i) * H + h) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32_sync(tmem + lane_off + TM_O + c * 32, o);
+        tmem_ld32_sync(o_addr + c * 32, o);
         if (i < L) {
           uint32_t w[16];
 #pragma unroll
@@ -367,7 +450,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, TM_COLS);
   }
@@ -418,11 +501,11 @@ bool prefill_tc_supported(const CacheView& cv) {
   return cv.dtype == RSWA_BF16 && cv.d == HD && encode_fn() != nullptr;
 }
 
-cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st,
+cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
                               const void* Q, const void* K, const void* V,
                               void* O, int64_t total_rows, cudaStream_t s) {
   if (!prefill_tc_supported(cv)) return cudaErrorNotSupported;
-  const int64_t end_row = st.row_off[0] + total_rows;
+  const int64_t end_row = st_in.row_off[0] + total_rows;
   if (end_row >= (int64_t(1) << 31)) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, cv.H, end_row) || !make_map(&mk, K, cv.H, end_row) ||
@@ -435,12 +518,20 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st,
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int tiles = st.tile_off[st.nseq];
-  if (tiles == 0) return cudaSuccess;
-  const int64_t grid = (int64_t)tiles * cv.H;
+  // Work units are pairs of 128-row tiles: tile_off counts pairs here.
+  SeqTable st = st_in;
+  int pairs = 0;
+  st.tile_off[0] = 0;
+  for (int i = 0; i < st.nseq; ++i) {
+    const int64_t L = st.m[i] + st.T;
+    pairs += (int)((L + 2 * BM - 1) / (2 * BM));
+    st.tile_off[i + 1] = pairs;
+  }
+  if (pairs == 0) return cudaSuccess;
+  const int64_t grid = (int64_t)pairs * cv.H;
   if (grid >= (int64_t(1) << 31)) return cudaErrorNotSupported;
   prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-      mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), tiles);
+      mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
   return cudaGetLastError();
 }
 
