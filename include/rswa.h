@@ -176,7 +176,7 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
  * Same arguments, layouts and result as rswa_decode_step_fused; the scratch
  * region of the cache buffer goes unused by this call.
  *   - Limit: the cache must need at most 4 MiB of scratch,
- *     B * H * max_chunks * (d + 2) * 4 bytes of partials plus (B * H + B) * 4
+ *     B * H * max_chunks * (d + 2) * 4 bytes of partials plus B * H * 4
  *     bytes of counters, each rounded up to 256 bytes; a larger cache is
  *     rejected with RSWA_ECAPACITY before anything runs.
  *   - The first call on a device looks up the array's device address (once

@@ -64,7 +64,7 @@ struct DeviceGuard {
 };
 
 struct Layout {
-  size_t m_off, t_off, err_off, k_off, v_off, part_off, cnt_bh_off, cnt_b_off;
+  size_t m_off, t_off, err_off, k_off, v_off, part_off, cnt_bh_off;
   size_t total;
   int chunk, max_chunks;
 };
@@ -106,10 +106,9 @@ Layout make_layout(int64_t m, int64_t n, int heads, int head_dim, int batch,
   L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
   size_t off = 0;
   L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);
-  L.t_off = off;      off = align_up(off + sizeof(int64_t) * batch);
+  L.t_off = off;      off = align_up(off + sizeof(int64_t) * batch * heads);
   L.err_off = off;    off = align_up(off + sizeof(int32_t));
   L.cnt_bh_off = off; off = align_up(off + sizeof(int32_t) * batch * heads);
-  L.cnt_b_off = off;  off = align_up(off + sizeof(int32_t) * batch);
   const size_t state_end = off;
   (void)state_end;
   L.k_off = off;
@@ -177,7 +176,6 @@ int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim, int batch,
   cv.err = reinterpret_cast<int32_t*>(base + L.err_off);
   cv.part = reinterpret_cast<float*>(base + L.part_off);
   cv.cnt_bh = reinterpret_cast<int32_t*>(base + L.cnt_bh_off);
-  cv.cnt_b = reinterpret_cast<int32_t*>(base + L.cnt_b_off);
   cv.B = batch;
   cv.H = heads;
   cv.d = head_dim;
@@ -331,7 +329,8 @@ static int read_state(rswa_cache* cache, int b, int64_t* m_b, int64_t* t_b) {
   if (cudaDeviceSynchronize() != cudaSuccess) return RSWA_ECUDA;
   if (cudaMemcpy(&m32, cache->cv.m_dev + b, sizeof(m32), cudaMemcpyDeviceToHost) !=
           cudaSuccess ||
-      cudaMemcpy(t_b, cache->cv.t_dev + b, sizeof(*t_b), cudaMemcpyDeviceToHost) !=
+      cudaMemcpy(t_b, cache->cv.t_dev + (size_t)b * cache->cv.H, sizeof(*t_b),
+                 cudaMemcpyDeviceToHost) !=
           cudaSuccess)
     return RSWA_ECUDA;
   *m_b = m32;

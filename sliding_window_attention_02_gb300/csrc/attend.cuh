@@ -96,13 +96,13 @@ __device__ __forceinline__ void attend_range(
       mx = fmaxf(mx, s[u]);
     }
     const float ref = (mx == -INFINITY) ? 0.f : mx;
-    const float alpha = exp2f(st.m - ref);
+    const float alpha = fast_exp2(st.m - ref);
     st.l *= alpha;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) st.acc[e] *= alpha;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const float p = exp2f(s[u] - ref);
+      const float p = fast_exp2(s[u] - ref);
       st.l += p;
       float vf[EPL];
       Elt<T>::widen(vr[u], vf);

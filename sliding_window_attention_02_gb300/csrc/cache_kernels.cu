@@ -5,6 +5,8 @@
 // no state transition", GeekNews, model architecture), rows m_cap..m_cap+n-1
 // the ring of output KV, where output j lives in slot j mod n (the queue of
 // capacity m + n that evicts its (m+1)-th entry).
+#include <vector>
+
 #include "rswa_device.cuh"
 
 namespace rswa {
@@ -20,9 +22,9 @@ prefill_cache_kernel(CacheView cv, SeqTable st, const T* __restrict__ K,
   const int64_t m_b = st.m[sl];
   const int64_t T_ = st.T;
   const int64_t keep = min(cv.n, T_);       // outputs kept in the ring
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    cv.m_dev[b] = (int32_t)m_b;
-    cv.t_dev[b] = T_;
+  if (blockIdx.x == 0) {
+    if (threadIdx.x == 0) cv.m_dev[b] = (int32_t)m_b;
+    for (int h = threadIdx.x; h < cv.H; h += blockDim.x) cv.t_dev[(size_t)b * cv.H + h] = T_;
   }
   const int D = cv.d, H = cv.H;
   const int nv = D * (int)sizeof(T) / 16;   // 16-byte vectors per head row
@@ -57,7 +59,7 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 append_kernel(CacheView cv, const T* __restrict__ k, const T* __restrict__ v) {
   const int b = blockIdx.x;
-  const int64_t t_b = cv.t_dev[b];
+  const int64_t t_b = cv.t_dev[(size_t)b * cv.H];
   const int64_t slot = t_b % cv.n;
   const int D = cv.d, H = cv.H;
   const int nv = D * (int)sizeof(T) / 16;
@@ -71,7 +73,7 @@ append_kernel(CacheView cv, const T* __restrict__ k, const T* __restrict__ v) {
     reinterpret_cast<uint4*>(out)[vi] = reinterpret_cast<const uint4*>(in)[vi];
   }
   __syncthreads();
-  if (threadIdx.x == 0) cv.t_dev[b] = t_b + 1;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) cv.t_dev[(size_t)b * H + h] = t_b + 1;
 }
 
 cudaError_t launch_prefill_cache(const CacheView& cv, const SeqTable& st,
@@ -101,7 +103,13 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
 
 cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
                          cudaStream_t s) {
-  return cudaMemcpyAsync(cv.t_dev, t_host, sizeof(int64_t) * cv.B,
+  // One copy of t_b per head; the caller synchronises before t_host and this
+  // staging array go away.
+  static thread_local std::vector<int64_t> per_head;
+  per_head.assign((size_t)cv.B * cv.H, 0);
+  for (int b = 0; b < cv.B; ++b)
+    for (int h = 0; h < cv.H; ++h) per_head[(size_t)b * cv.H + h] = t_host[b];
+  return cudaMemcpyAsync(cv.t_dev, per_head.data(), sizeof(int64_t) * per_head.size(),
                          cudaMemcpyHostToDevice, s);
 }
 

@@ -33,9 +33,9 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   const int cr = (int)((cv.n + chunk - 1) / chunk);
   const int nch = cp + cr;
   if (c >= nch) return;
-  const int64_t t_b = cv.t_dev[b];
-
   const size_t bh = (size_t)b * cv.H + h;
+  const int64_t t_b = cv.t_dev[bh];
+
   const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
   const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
   const T* kn = FUSED ? knew + bh * D : nullptr;
@@ -101,7 +101,7 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   float Ls = 0.f, A = 0.f;
 #pragma unroll
   for (int w = 0; w < NW; ++w) {
-    const float sc = exp2f(s_m[w] - ref);
+    const float sc = fast_exp2(s_m[w] - ref);
     Ls += s_l[w] * sc;
     if (tid < D) A += s_acc[w][tid] * sc;
   }
@@ -125,7 +125,7 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     const float r2 = (Mx == -INFINITY) ? 0.f : Mx;
     float Lt = 0.f, At = 0.f;
     for (int k = 0; k < nch; ++k) {
-      const float sc = exp2f(__ldcg(P + k * (D + 2)) - r2);
+      const float sc = fast_exp2(__ldcg(P + k * (D + 2)) - r2);
       Lt += __ldcg(P + k * (D + 2) + 1) * sc;
       if (tid < D) At += __ldcg(P + k * (D + 2) + 2 + tid) * sc;
     }
@@ -133,14 +133,9 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     if (tid == 0) {
       if (lse) lse[bh] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;
       cv.cnt_bh[bh] = 0;
-    }
-  }
-  if (FUSED && tid == 0) {
-    // The last CTA of sequence b (over all heads) advances t_b.  Every other
-    // CTA of b read t_b before its own arrival.
-    if (atomicAdd(&cv.cnt_b[b], 1) == cv.H * nch - 1) {
-      cv.cnt_b[b] = 0;
-      cv.t_dev[b] = t_b + 1;
+      // The last CTA of (b, h) advances this head's t_b; every other CTA of
+      // (b, h) read it before its own arrival.
+      if (FUSED) cv.t_dev[bh] = t_b + 1;
     }
   }
 }
@@ -162,7 +157,7 @@ decode_small_kernel(CacheView cv, const T* __restrict__ q,
   griddep_wait();
   griddep_launch_dependents();
   const int64_t m_b = cv.m_dev[b];
-  const int64_t t_b = cv.t_dev[b];
+  const int64_t t_b = cv.t_dev[bh];
   const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
   const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
   const T* kn = FUSED ? knew + bh * D : nullptr;
@@ -210,22 +205,16 @@ decode_small_kernel(CacheView cv, const T* __restrict__ q,
     float Ls = 0.f, A = 0.f;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float sc = exp2f(s_m[w] - ref);
+      const float sc = fast_exp2(s_m[w] - ref);
       Ls += s_l[w] * sc;
       A += s_acc[w][tid] * sc;
     }
     o[bh * D + tid] = (T)(Ls > 0.f ? A / Ls : 0.f);
     if (tid == 0 && lse) lse[bh] = Ls > 0.f ? (ref + log2f(Ls)) * kLn2 : -INFINITY;
   }
-  if (FUSED && tid == 0) {
-    // The last head of sequence b to finish advances t_b; every other head
-    // read t_b before its own arrival.
-    __threadfence();
-    if (atomicAdd(&cv.cnt_b[b], 1) == cv.H - 1) {
-      cv.cnt_b[b] = 0;
-      cv.t_dev[b] = t_b + 1;
-    }
-  }
+  // This CTA is the only reader of its head's t_b (read before the
+  // __syncthreads above): advance it.
+  if (FUSED && tid == 0) cv.t_dev[bh] = t_b + 1;
 }
 
 constexpr int kSmallWarps = 16;

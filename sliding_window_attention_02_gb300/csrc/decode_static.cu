@@ -47,7 +47,7 @@ size_t static_scratch_need(const CacheView& cv, size_t* part_bytes,
                            size_t* cnt_bytes) {
   *part_bytes = align256(sizeof(float) * (size_t)cv.B * cv.H * cv.max_chunks *
                          (cv.d + 2));
-  *cnt_bytes = align256(sizeof(int32_t) * ((size_t)cv.B * cv.H + cv.B));
+  *cnt_bytes = align256(sizeof(int32_t) * (size_t)cv.B * cv.H);
   return *part_bytes + *cnt_bytes;
 }
 
@@ -69,7 +69,6 @@ cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
   CacheView sv = cv;
   sv.part = reinterpret_cast<float*>(b);
   sv.cnt_bh = reinterpret_cast<int32_t*>(b + part_bytes);
-  sv.cnt_b = sv.cnt_bh + (size_t)cv.B * cv.H;
   e = cudaMemsetAsync(sv.cnt_bh, 0, cnt_bytes, s);
   if (e != cudaSuccess) return e;
   return launch_decode(sv, q, k, v, o, lse, true, s);

@@ -23,6 +23,14 @@ __device__ __forceinline__ void flag_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz: relative error about
+// 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Programmatic dependent launch: wait for the preceding grid of the stream
 // (a no-op when the kernel was not launched as a dependent), and allow the
 // next grid to begin launching.
@@ -100,8 +108,8 @@ struct SoftmaxState {
   __device__ __forceinline__ void merge(float m2, float l2, const float* a2) {
     const float mn = fmaxf(m, m2);
     const float ref = (mn == -INFINITY) ? 0.f : mn;
-    const float s1 = exp2f(m - ref);
-    const float s2 = exp2f(m2 - ref);
+    const float s1 = fast_exp2(m - ref);
+    const float s2 = fast_exp2(m2 - ref);
     l = l * s1 + l2 * s2;
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = acc[e] * s1 + a2[e] * s2;

@@ -14,12 +14,14 @@ constexpr int kDecodeThreads = 128;     // threads per decode CTA
 // Device view of a cache buffer.  All regions live in the caller's buffer.
 //   K, V    slabs [B][H][slab_rows][d], slab_rows = m_cap + n: rows
 //           0..m_cap-1 are the prefix region, rows m_cap..m_cap+n-1 the ring.
-//   m_dev   int32 [B]  prefix length m_b
-//   t_dev   int64 [B]  outputs appended t_b
-//   err     int32 [1]  first device-side error code (0 = none)
+//   m_dev   int32 [B]     prefix length m_b
+//   t_dev   int64 [B][H]  outputs appended t_b, one copy per head so that a
+//                         fused decode step advances each head's copy
+//                         without cross-head synchronisation; all copies
+//                         of a sequence are equal between calls
+//   err     int32 [1]     first device-side error code (0 = none)
 //   part    float [B][H][max_chunks][d + 2]  split-K partials (m, l, acc)
 //   cnt_bh  int32 [B][H]  CTAs of (b, h) that have published a partial
-//   cnt_b   int32 [B]     CTAs of sequence b done (fused step: advances t_b)
 struct CacheView {
   void* K;
   void* V;
@@ -28,7 +30,6 @@ struct CacheView {
   int32_t* err;
   float* part;
   int32_t* cnt_bh;
-  int32_t* cnt_b;
   int B, H, d, dtype;
   int64_t m_cap, n, slab_rows;
   int chunk;       // keys per decode CTA
