@@ -140,18 +140,23 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   }
 }
 
-// Small-batch decode: one CTA of NW warps per (b, h) streams the prefix and
-// the ring as one logical key range, merges its warps in shared memory and
-// writes o directly - no partials, no second pass.  Used when the whole cache
-// of a head is a few CTA-iterations long and there are few heads in flight,
-// where the split-K combine would only add latency.
+constexpr uint32_t kMaxClusterSize = 8;
+
+// Small-batch decode: a thread-block cluster of CL CTAs (NW warps each) per
+// (b, h).  The prefix rows and the filled ring slots form one logical key
+// range, split evenly over the cluster; each CTA merges its warps in shared
+// memory, and CTA rank 0 combines the CL partials through distributed shared
+// memory between two cluster barriers - no global partials, no atomics.  Used
+// when few heads are in flight and every head's cache is short, where the
+// global split-K combine would only add latency.
 template <typename T, int D, bool FUSED, int NW>
 __global__ void __launch_bounds__(NW * 32)
-decode_small_kernel(CacheView cv, const T* __restrict__ q,
-                    const T* __restrict__ knew, const T* __restrict__ vnew,
-                    T* __restrict__ o, float* __restrict__ lse) {
+decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
+                      const T* __restrict__ knew, const T* __restrict__ vnew,
+                      T* __restrict__ o, float* __restrict__ lse) {
   using C = AttendCfg<T, D>;
-  const int h = blockIdx.x, b = blockIdx.y;
+  const uint32_t rank = cluster_rank(), CL = cluster_size();
+  const int h = blockIdx.x / CL, b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t bh = (size_t)b * cv.H + h;
   griddep_wait();
@@ -166,27 +171,37 @@ decode_small_kernel(CacheView cv, const T* __restrict__ q,
   int64_t sub = -1;
   if (FUSED) {
     sub = cv.m_cap + t_b % cv.n;
-    T* Kw = static_cast<T*>(cv.K) + (bh * cv.slab_rows + sub) * D;
-    T* Vw = static_cast<T*>(cv.V) + (bh * cv.slab_rows + sub) * D;
-    constexpr int NV = D * sizeof(T) / 16;
-    for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
-      if (i < NV)
-        reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(kn)[i];
-      else
-        reinterpret_cast<uint4*>(Vw)[i - NV] = reinterpret_cast<const uint4*>(vn)[i - NV];
+    if (rank == 0) {
+      // No CTA of this launch reads slot sub from the slab.
+      T* Kw = static_cast<T*>(cv.K) + (bh * cv.slab_rows + sub) * D;
+      T* Vw = static_cast<T*>(cv.V) + (bh * cv.slab_rows + sub) * D;
+      constexpr int NV = D * sizeof(T) / 16;
+      for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
+        if (i < NV)
+          reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(kn)[i];
+        else
+          reinterpret_cast<uint4*>(Vw)[i - NV] = reinterpret_cast<const uint4*>(vn)[i - NV];
+      }
     }
   }
+  // This CTA's share of the logical keys 0..m_b+filled-1 (0..m_b-1 ->
+  // prefix rows, m_b.. -> ring rows m_cap..).
+  const int64_t total = m_b + filled;
+  const int64_t per = (total + CL - 1) / CL;
+  const int64_t j0 = min(total, (int64_t)rank * per);
+  const int64_t j1 = min(total, j0 + per);
   float qf[C::EPL];
   load_q_frag<T, D>(q + bh * D, lane, qf);
   SoftmaxState<C::EPL> st;
   st.init();
-  // logical keys 0..m_b-1 -> prefix rows, m_b.. -> ring rows m_cap..
-  attend_range<T, D>(qf, Kb, Vb, D, 0, m_b + filled, (int64_t)warp * C::KEYS_WARP,
+  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
                      (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane, st, m_b,
                      cv.m_cap - m_b);
   merge_groups<T, D>(st);
   __shared__ float s_m[NW], s_l[NW];
   __shared__ float s_acc[NW][D];
+  __shared__ float p_ml[2];          // this CTA's partial, read by rank 0
+  __shared__ float p_acc[D];
   if (lane < C::LPK) {
 #pragma unroll
     for (int e = 0; e < C::EPL; ++e) s_acc[warp][lane * C::EPL + e] = st.acc[e];
@@ -209,32 +224,88 @@ decode_small_kernel(CacheView cv, const T* __restrict__ q,
       Ls += s_l[w] * sc;
       A += s_acc[w][tid] * sc;
     }
-    o[bh * D + tid] = (T)(Ls > 0.f ? A / Ls : 0.f);
-    if (tid == 0 && lse) lse[bh] = Ls > 0.f ? (ref + log2f(Ls)) * kLn2 : -INFINITY;
+    p_acc[tid] = A;
+    if (tid == 0) {
+      p_ml[0] = M;
+      p_ml[1] = Ls;
+    }
   }
-  // This CTA is the only reader of its head's t_b (read before the
-  // __syncthreads above): advance it.
-  if (FUSED && tid == 0) cv.t_dev[bh] = t_b + 1;
+  cluster_sync();                    // partials of every CTA visible
+  if (rank == 0 && tid < D) {
+    float Mr[kMaxClusterSize], Lr[kMaxClusterSize], Ar[kMaxClusterSize];
+    float M = -INFINITY;
+#pragma unroll
+    for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
+      Mr[r] = -INFINITY;
+      Lr[r] = Ar[r] = 0.f;
+      if (r < CL) {
+        Mr[r] = ld_dsmem(&p_ml[0], r);
+        Lr[r] = ld_dsmem(&p_ml[1], r);
+        Ar[r] = ld_dsmem(&p_acc[tid], r);
+      }
+      M = fmaxf(M, Mr[r]);
+    }
+    const float ref = (M == -INFINITY) ? 0.f : M;
+    float Ls = 0.f, A = 0.f;
+#pragma unroll
+    for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
+      const float sc = fast_exp2(Mr[r] - ref);
+      Ls += Lr[r] * sc;
+      A += Ar[r] * sc;
+    }
+    o[bh * D + tid] = (T)(Ls > 0.f ? A / Ls : 0.f);
+    if (tid == 0) {
+      if (lse) lse[bh] = Ls > 0.f ? (ref + log2f(Ls)) * kLn2 : -INFINITY;
+      // Every CTA of the cluster read t_b before the first cluster barrier.
+      if (FUSED) cv.t_dev[bh] = t_b + 1;
+    }
+  }
+  cluster_sync();                    // rank 0 done reading remote memory
 }
 
-constexpr int kSmallWarps = 16;
+constexpr int kClusterWarps = 8;
+constexpr int kMaxCluster = (int)kMaxClusterSize;
 
 // Launch with programmatic stream serialization so that a decode kernel may
-// begin launching while the previous kernel of the stream drains.
+// begin launching while the previous kernel of the stream drains; with a
+// cluster dimension when cluster > 0.
 template <typename K, typename... Args>
-static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t s,
-                              Args... args) {
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, int cluster,
+                              cudaStream_t s, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 0) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Keys one CTA of the cluster path covers per iteration of its warps.
+static int64_t cluster_keys_per_iter(const CacheView& cv) {
+  const int epl = cv.dtype == RSWA_F32 ? 4 : 8;
+  const int kpw = 32 / (cv.d / epl);
+  return (int64_t)kClusterWarps * kpw * RSWA_DECODE_UNROLL;
+}
+
+// Cluster size: enough CTAs for one iteration per CTA, at most 8.
+static int cluster_size_for(const CacheView& cv) {
+  const int64_t per = cluster_keys_per_iter(cv);
+  const int64_t want = (cv.m_cap + cv.n + per - 1) / per;
+  return (int)(want < 1 ? 1 : (want > kMaxCluster ? kMaxCluster : want));
 }
 
 template <typename T, int D>
@@ -247,34 +318,35 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
   T* oo = (T*)o;
   cudaError_t e;
   if (decode_use_small(cv)) {
-    dim3 grid(cv.H, cv.B);
+    const int cl = cluster_size_for(cv);
+    dim3 grid(cv.H * cl, cv.B);
     if (fused)
-      e = launch_pdl(decode_small_kernel<T, D, true, kSmallWarps>, grid,
-                     dim3(kSmallWarps * 32), s, cv, qq, kk, vv, oo, lse);
+      e = launch_pdl(decode_cluster_kernel<T, D, true, kClusterWarps>, grid,
+                     dim3(kClusterWarps * 32), cl, s, cv, qq, kk, vv, oo, lse);
     else
-      e = launch_pdl(decode_small_kernel<T, D, false, kSmallWarps>, grid,
-                     dim3(kSmallWarps * 32), s, cv, qq, (const T*)nullptr,
+      e = launch_pdl(decode_cluster_kernel<T, D, false, kClusterWarps>, grid,
+                     dim3(kClusterWarps * 32), cl, s, cv, qq, (const T*)nullptr,
                      (const T*)nullptr, oo, lse);
   } else {
     dim3 grid(cv.max_chunks, cv.H, cv.B);
     if (fused)
-      e = launch_pdl(decode_kernel<T, D, true>, grid, dim3(kDecodeThreads), s, cv,
-                     qq, kk, vv, oo, lse);
+      e = launch_pdl(decode_kernel<T, D, true>, grid, dim3(kDecodeThreads), 0, s,
+                     cv, qq, kk, vv, oo, lse);
     else
-      e = launch_pdl(decode_kernel<T, D, false>, grid, dim3(kDecodeThreads), s, cv,
-                     qq, (const T*)nullptr, (const T*)nullptr, oo, lse);
+      e = launch_pdl(decode_kernel<T, D, false>, grid, dim3(kDecodeThreads), 0, s,
+                     cv, qq, (const T*)nullptr, (const T*)nullptr, oo, lse);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// One CTA per head when every head's cache is at most 4 CTA-iterations of
-// keys and all heads fit in one wave of CTAs.
+// The cluster path when every head's cache fits one iteration of a cluster
+// of at most 8 CTAs (two for wider clusters' worth of keys is the split-K
+// path's job) and all clusters fit in one wave of the 152 SMs.
 bool decode_use_small(const CacheView& cv) {
-  const int64_t keys_per_iter = (int64_t)kSmallWarps * 32 *
-                                (cv.dtype == RSWA_F32 ? 4 : 8) / cv.d *
-                                RSWA_DECODE_UNROLL;
-  return (int64_t)cv.B * cv.H <= 152 && cv.m_cap + cv.n <= 4 * keys_per_iter;
+  const int64_t per = cluster_keys_per_iter(cv);
+  return cv.m_cap + cv.n <= kMaxCluster * per &&
+         (int64_t)cv.B * cv.H * cluster_size_for(cv) <= 152 * 2;
 }
 
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
