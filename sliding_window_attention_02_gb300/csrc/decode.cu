@@ -14,8 +14,11 @@
 
 namespace rswa {
 
+// At least 5 resident CTAs per SM: measured best on GB300 for the batched
+// and long-output workloads (it also steers the compiler to issue a warp's
+// loads ahead of their use).
 template <typename T, int D, bool FUSED>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 5)
 decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
               const T* __restrict__ vnew, T* __restrict__ o,
               float* __restrict__ lse) {
