@@ -443,6 +443,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms, dist=None, device=None):
+    """Step time of the whole job: the slowest rank's (timing reduction only;
+    the data path has no collective)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def job_throughput(tokens_per_rank, world_size, ms):
+    """Whole-job tokens/s: every rank runs its own replica of the workload
+    (weak scaling), so the job processes world_size x the tokens of one."""
+    return tokens_per_rank * world_size / (ms * 1e-3)
+
+
 def main_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -533,15 +551,10 @@ def main_ours(args):
         dist.barrier()
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     dec_ms = [b.elapsed_time(c) for _, b, c in ev]
-    ms = statistics.mean(step_ms)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = t.item()
+    ms = max_over_ranks(statistics.mean(step_ms), dist, dev)
     clocks = clk.summary()
     cache_bytes = sp["cache"].cache_bytes(0)      # C(T) after the loop
-    tokens = w.batch * w.T * ws
-    value = tokens / (ms * 1e-3)
+    value = job_throughput(w.batch * w.T, ws, ms)
 
     # dominant kernel: fused decode (6000 launches per step)
     per_launch_ms = statistics.mean(dec_ms) / w.T
