@@ -146,21 +146,23 @@ class ClockSampler:
 # workloads (setup shared with the full-size GPU tests)
 # ---------------------------------------------------------------------------
 
-def setup_single_page(dev, seed=0, pinned_inputs=False):
+def setup_single_page(dev, seed=0, n=None):
     """Cache and inputs of the single-page workload, plus CUDA graphs for the
-    prefix prefill and the 6000-step fused decode loop."""
+    prefix prefill and the 6000-step fused decode loop.  `n` overrides the
+    window (n >= T gives the standard full-cache MHA baseline)."""
     import torch
     import sliding_window_attention_02_gb300 as rswa
     import workloads
     w = workloads.WORKLOADS["single_page_bf16"]
-    B, H, d, m, n, T = w.batch, w.heads, w.head_dim, w.m, w.n, w.T
+    B, H, d, m, T = w.batch, w.heads, w.head_dim, w.m, w.T
+    n = w.n if n is None else n
     Q, K, V = workloads.qkv(m + T, H, d, seed, w.std, torch.bfloat16, device=dev)
     cache = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
     Op = torch.empty(m, H, d, dtype=torch.bfloat16, device=dev)
     Od = torch.empty(T, B, H, d, dtype=torch.bfloat16, device=dev)
     s = torch.cuda.Stream(device=dev)
-    st = {"w": w, "Q": Q, "K": K, "V": V, "cache": cache, "Op": Op, "Od": Od,
-          "stream": s}
+    st = {"w": w, "n": n, "Q": Q, "K": K, "V": V, "cache": cache, "Op": Op,
+          "Od": Od, "stream": s}
 
     def prefill():
         cache.prefill(Q[:m], K[:m], V[:m], Op, [m], 0, stream=s)
@@ -286,6 +288,58 @@ def events_time(fn, stream, iters, flush=None):
 GRAPH_STEPS = 16
 
 
+def run_mha_baseline(dev, quick=False):
+    """R-SWA (n = 128) against the standard full cache (n = T = 6000, i.e.
+    every output stays visible: plain causal attention) on the single-page
+    shape, through the same kernels.  Per-step decode latency at several t,
+    the live cache size at each t, and the whole 6000-step decode loop."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    B, H, d, m, T = w.batch, w.heads, w.head_dim, w.m, w.T
+    s = torch.cuda.Stream(device=dev)
+    Q, K, V = workloads.qkv(m + T, H, d, 0, w.std, torch.bfloat16, device=dev)
+    steps = workloads.qkv(16, H, d, 77, w.std, torch.bfloat16, device=dev)
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    points = []
+    caches = {}
+    for name, n in (("rswa", w.n), ("mha", T)):
+        c = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+        c.prefill(None, K, V, None, [m], T, stream=s)   # all 6000 outputs
+        caches[name] = c
+    for t in ((512, 2048, 5984) if quick else (128, 512, 1024, 2048, 4096, 5984)):
+        row = {"t": t}
+        for name, c in caches.items():
+            c.set_t([t], stream=s)
+            idx = [0]
+
+            def step():
+                i = idx[0] % 16
+                idx[0] += 1
+                c.decode_step_fused(steps[0][i][None], steps[1][i][None],
+                                    steps[2][i][None], o, stream=s)
+            row[name + "_us"] = round(1e3 * graph_step_ms(step, s, 16, 3), 3)
+            c.set_t([t], stream=s)
+            row[name + "_cache_bytes"] = c.cache_bytes(0)
+        points.append(row)
+    del caches
+    loops = {}
+    for name, n in (("rswa", w.n), ("mha", T)):
+        sp = setup_single_page(dev, n=n)
+        with torch.cuda.stream(sp["stream"]):
+            sp["g_prefill"].replay()
+        ts = events_time(lambda: sp["g_decode"].replay(), sp["stream"],
+                         1 if quick else 3)
+        loops[name] = T / (statistics.mean(ts) * 1e-3)
+        del sp
+    return {"workload": "B1 H10 d128 m288 bf16 decode: R-SWA n=128 vs full "
+                        "cache n=6000 (standard MHA), same kernels",
+            "points": points,
+            "loop_tokens_per_s": {k: round(v, 1) for k, v in loops.items()},
+            "loop_speedup": round(loops["rswa"] / loops["mha"], 3)}
+
+
 def graph_step_ms(step, stream, nsteps, iters):
     """Mean ms per step: `nsteps` steps captured in one CUDA graph, replayed
     `iters` times (after 2 warm-up replays), timed with events on `stream`.
@@ -362,6 +416,9 @@ def run_extras(dev, peaks, quick=False):
         "algorithmic_bytes": nbytes, "points": rows,
         "latency_spread": round((max(us) - min(us)) / statistics.mean(us), 4)}
     del sw
+    # standard-MHA baseline (the pages' comparison) -------------------------
+    out["mha_baseline"] = run_mha_baseline(dev, quick)
+    torch.cuda.empty_cache()
     # multi-page prefill ----------------------------------------------------
     pf = setup_prefill(dev, layers=2 if quick else None)
     w = pf["w"]

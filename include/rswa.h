@@ -160,6 +160,23 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
                                     float* lse, void* stream);
 
 /*
+ * Decode a block of `block` consecutive output tokens per sequence in one
+ * call (1 <= block <= n): q, k, v, o are [B][block][H][d] for outputs
+ * t_b .. t_b + block - 1; lse (may be NULL) is [B][block][H] float32.
+ * Output t_b + i attends to the prefix, to the cached outputs of its window
+ * j in [max(0, t_b + i - n + 1), t_b), and to block tokens 0..i - exactly
+ * what `block` single steps would give (N(t) = P U D_n(t), "Unlimited-OCR
+ * deep dive" pseudo-code block).  The block's keys and values are then
+ * appended (slots (t_b + i) mod n) and t_b advances by `block`.  For
+ * verifying drafted tokens or prefilling output text into an existing cache.
+ * Errors: RSWA_EINVAL (block outside 1..n, null or misaligned pointers),
+ * RSWA_EHANDLE, RSWA_ECUDA.
+ */
+RSWA_API int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
+                               const void* v, int64_t block, void* o,
+                               float* lse, void* stream);
+
+/*
  * rswa_decode_step_fused without scratch from the cache buffer.  (Not part of
  * the method on the pages: it has no counterpart there.)
  *

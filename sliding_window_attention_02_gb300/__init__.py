@@ -21,7 +21,7 @@ __all__ = [
     "rswa_strerror", "rswa_cache_footprint", "rswa_cache_create",
     "rswa_cache_destroy", "rswa_prefill", "rswa_append_kv",
     "rswa_decode_step", "rswa_decode_step_fused",
-    "rswa_decode_step_fused_static", "rswa_cache_bytes",
+    "rswa_decode_step_fused_static", "rswa_decode_block", "rswa_cache_bytes",
     "rswa_cache_len", "rswa_cache_get_t", "rswa_cache_set_t",
     "rswa_sync_status", "rswa_debug_fail_next_cuda", "rswa_cache_kv_offsets",
     "RswaCache",
@@ -53,6 +53,8 @@ _SIGNATURES = {
                                         _c_vp, _c_vp]),
     "rswa_decode_step_fused_static": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp,
                                                _c_vp, _c_vp, _c_vp]),
+    "rswa_decode_block": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp,
+                                   _c_vp, _c_vp]),
     "rswa_cache_bytes": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_size)]),
     "rswa_cache_len": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_i64)]),
     "rswa_cache_get_t": (_c_int, [_c_vp, _c_int, ctypes.POINTER(_c_i64)]),
@@ -191,6 +193,14 @@ def rswa_decode_step_fused_static(handle, q, k, v, o, lse=None,
            "rswa_decode_step_fused_static")
 
 
+def rswa_decode_block(handle, q, k, v, o, lse=None, stream=None) -> None:
+    """q, k, v, o: [B][block][H][d]; lse: [B][block][H] or None."""
+    _check(load().rswa_decode_block(handle, _ptr(q), _ptr(k), _ptr(v),
+                                    int(q.shape[1]), _ptr(o), _ptr(lse),
+                                    _stream(stream)),
+           "rswa_decode_block")
+
+
 def rswa_cache_bytes(handle, b: int) -> int:
     out = _c_size(0)
     _check(load().rswa_cache_bytes(handle, b, ctypes.byref(out)),
@@ -265,6 +275,9 @@ class RswaCache:
 
     def decode_step_fused(self, q, k, v, o, lse=None, stream=None):
         rswa_decode_step_fused(self.handle, q, k, v, o, lse, stream)
+
+    def decode_block(self, q, k, v, o, lse=None, stream=None):
+        rswa_decode_block(self.handle, q, k, v, o, lse, stream)
 
     def cache_bytes(self, b):
         return rswa_cache_bytes(self.handle, b)

@@ -301,6 +301,21 @@ int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
                                  static_cast<cudaStream_t>(stream)));
 }
 
+int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
+                      const void* v, int64_t block, void* o, float* lse,
+                      void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (block < 1 || block > cache->cv.n) return RSWA_EINVAL;
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(o))
+    return RSWA_EINVAL;
+  if (injected_failure()) return RSWA_ECUDA;
+  DeviceGuard g(cache->device);
+  if (!g.ok) return RSWA_ECUDA;
+  return status_of(launch_decode_block(cache->cv, q, k, v, block, o, lse,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
                                   const void* k, const void* v, void* o,
                                   float* lse, void* stream) {

@@ -55,6 +55,9 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
 cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
                          cudaStream_t s);
 bool decode_use_small(const CacheView& cv);
+cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
+                                const void* v, int64_t block, void* o, float* lse,
+                                cudaStream_t s);
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           const void* v, void* o, float* lse, bool fused,
                           cudaStream_t s);

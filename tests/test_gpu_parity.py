@@ -171,6 +171,8 @@ DECODE_CASES = [
     ([64, 300, 5], 16, 40, 2, 128),
     ([100], 7, 23, 1, 64),
     ([1500], 128, 140, 1, 128),
+    ([300], 2048, 200, 2, 128),   # n >= T: the full-cache (MHA) baseline
+    ([64], 512, 300, 2, 128),     # n >= T on the cluster path
 ]
 
 
@@ -209,6 +211,51 @@ def test_bf16_decode(cuda_lib, case, fused):
         assert np.abs(lse_got[:, b] - refs[b][1][m:]).max() <= 1e-3
         assert cache.get_t(b) == T
         assert cache.cache_len(b) == oracle.cache_len(m, n, T)
+
+
+BLOCK_CASES = [
+    # (m_list, n, T, block sizes in order, H, d)
+    ([288], 128, 0, [5, 1, 34, 128, 7, 100], 2, 128),
+    ([40, 0, 300], 16, 0, [16, 3, 9, 16], 2, 128),
+    ([17], 8, 0, [8, 8, 3], 1, 64),
+]
+
+
+@pytest.mark.parametrize("case", BLOCK_CASES, ids=lambda c: f"m{c[0]}n{c[1]}")
+def test_bf16_decode_block(cuda_lib, case):
+    """Blocks of consecutive outputs (speculative-verify shape) must equal
+    the prefill rows m + t .. m + t + k - 1 of the same sequence."""
+    rswa = cuda_lib
+    m_list, n, _, blocks, H, d = case
+    B = len(m_list)
+    T = sum(blocks)
+    Q, K, V = make_seq(m_list, T, H, d, 1, seed=9)
+    refs = oracle_prefill(Q, K, V, m_list, T, n)
+    offs = np.cumsum([0] + [m + T for m in m_list])
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, 0)
+    t = 0
+    for kb in blocks:
+        rows = [[offs[b] + m_list[b] + t + i for i in range(kb)] for b in range(B)]
+        q, k, v = (torch.stack([x[r] for r in rows]).contiguous().cuda()
+                   for x in (Q, K, V))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, kb, H, device="cuda")
+        cache.decode_block(q, k, v, o, lse)
+        torch.cuda.synchronize()
+        for b, m in enumerate(m_list):
+            assert_close(f64(o[b]), refs[b][0][m + t:m + t + kb], 1,
+                         f"block at t={t} seq {b}")
+            assert np.abs(f64(lse[b]) - refs[b][1][m + t:m + t + kb]).max() <= 1e-3
+        t += kb
+        for b in range(B):
+            assert cache.get_t(b) == t
+    assert cache.sync_status() == 0
+    with pytest.raises(rswa.RswaError):
+        big = torch.zeros(B, n + 1, H, d, dtype=torch.bfloat16, device="cuda")
+        cache.decode_block(big, big, big, big)
 
 
 def test_ring_sentinels_bit_exact(cuda_lib):
