@@ -288,6 +288,38 @@ def events_time(fn, stream, iters, flush=None):
 GRAPH_STEPS = 16
 
 
+def run_long_prefix_decode(dev, peaks):
+    """B 1, H 10, d 128, n 128: per-step fused decode latency for prefixes of
+    4, 16 and 40 pages (the decode that follows a multi-page prefill)."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    H, d, n = 10, 128, 128
+    s = torch.cuda.Stream(device=dev)
+    steps = workloads.qkv(16, H, d, 5, 1.0, torch.bfloat16, device=dev)
+    o = torch.empty(1, H, d, dtype=torch.bfloat16, device=dev)
+    rows = []
+    for m in (1056, 4128, 10272):
+        _, K, V = workloads.qkv(m + n, H, d, 0, 1.0, torch.bfloat16, device=dev)
+        c = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+        c.prefill(None, K, V, None, [m], n, stream=s)
+        idx = [0]
+
+        def step():
+            i = idx[0] % 16
+            idx[0] += 1
+            c.decode_step_fused(steps[0][i][None], steps[1][i][None],
+                                steps[2][i][None], o, stream=s)
+        ms = graph_step_ms(step, s, 16, 5)
+        nbytes = H * d * 2 * (2 * (m + n) + 4)
+        rows.append({"m": m, "us_per_step": round(ms * 1e3, 2),
+                     "GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1)})
+        del c, K, V
+    return {"workload": "B1 H10 d128 n128 bf16 fused decode, prefix of 4/16/40 "
+                        "pages (latency-bound: 2-53 MB per step)",
+            "points": rows}
+
+
 def run_mha_baseline(dev, quick=False):
     """R-SWA (n = 128) against the standard full cache (n = T = 6000, i.e.
     every output stays visible: plain causal attention) on the single-page
@@ -416,6 +448,9 @@ def run_extras(dev, peaks, quick=False):
         "algorithmic_bytes": nbytes, "points": rows,
         "latency_spread": round((max(us) - min(us)) / statistics.mean(us), 4)}
     del sw
+    # one sequence decoding over a long prefix (after a multi-page prefill) --
+    out["long_prefix_decode"] = run_long_prefix_decode(dev, peaks)
+    torch.cuda.empty_cache()
     # standard-MHA baseline (the pages' comparison) -------------------------
     out["mha_baseline"] = run_mha_baseline(dev, quick)
     torch.cuda.empty_cache()

@@ -83,13 +83,21 @@ int valid_shape(int64_t m, int64_t n, int heads, int head_dim, int batch,
 #define RSWA_DECODE_CTAS_PER_SM 32
 #endif
 
-// Keys per decode CTA: a power of two >= 64, chosen so that the largest
-// possible decode grid holds about RSWA_DECODE_CTAS_PER_SM CTAs per SM of a
-// 152-SM GB300.
+// Keys per decode CTA, a power of two.  Many heads (more than the 152 SMs):
+// sized so that the largest possible decode grid holds about
+// RSWA_DECODE_CTAS_PER_SM CTAs per SM.  Few heads: about 40 chunks per head,
+// 128..256 keys each (measured best on GB300 for one sequence with a 1K-10K
+// key cache; shorter caches take the cluster path).
 int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
 #ifdef RSWA_DECODE_CHUNK
   return RSWA_DECODE_CHUNK;
 #endif
+  if ((int64_t)batch * heads <= 152) {
+    const int64_t want = (m + n + 39) / 40;
+    int c = 128;
+    while (c < want && c < 256) c <<= 1;
+    return c;
+  }
   const int64_t keys = (int64_t)batch * heads * (m + n);
   const int64_t target = 152 * RSWA_DECODE_CTAS_PER_SM;
   int64_t want = (keys + target - 1) / target;

@@ -173,6 +173,8 @@ DECODE_CASES = [
     ([1500], 128, 140, 1, 128),
     ([300], 2048, 200, 2, 128),   # n >= T: the full-cache (MHA) baseline
     ([64], 512, 300, 2, 128),     # n >= T on the cluster path
+    # more than 152 heads in flight: the split-K kernel with its global combine
+    ([37 * (i % 7) + 3 for i in range(20)], 16, 12, 8, 128),
 ]
 
 
