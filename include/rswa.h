@@ -100,6 +100,24 @@ RSWA_API int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim,
                                int batch, int dtype, void* device_buf,
                                size_t buf_bytes, rswa_cache** out);
 
+/*
+ * Grouped-query variants (not on the pages, which name standard MHA as the
+ * baseline): `heads` query heads share `kv_heads` key/value heads
+ * (heads % kv_heads == 0); query head h reads KV head h / (heads / kv_heads).
+ * The cache then stores kv_heads slabs, and every K/V tensor of the other
+ * calls has kv_heads heads ([rows][kv_heads][d], [B][kv_heads][d]) while
+ * Q, O, q, o, lse keep `heads`.  kv_heads == heads is exactly
+ * rswa_cache_footprint / rswa_cache_create.  Errors as theirs, plus
+ * RSWA_EINVAL when kv_heads does not divide heads.
+ */
+RSWA_API int rswa_cache_footprint_gqa(int64_t m, int64_t n, int heads,
+                                      int kv_heads, int head_dim, int batch,
+                                      int dtype, size_t* out_bytes);
+RSWA_API int rswa_cache_create_gqa(int64_t m, int64_t n, int heads,
+                                   int kv_heads, int head_dim, int batch,
+                                   int dtype, void* device_buf,
+                                   size_t buf_bytes, rswa_cache** out);
+
 /* Free the host handle (not the device buffer).  Later use of the handle
  * returns RSWA_EHANDLE. */
 RSWA_API int rswa_cache_destroy(rswa_cache* cache);
@@ -124,6 +142,20 @@ RSWA_API int rswa_cache_destroy(rswa_cache* cache);
 RSWA_API int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
                           const void* V, void* O, const int64_t* m_per_seq,
                           int64_t T, void* stream);
+
+/*
+ * rswa_prefill with a number of output rows per sequence: t_per_seq is a
+ * HOST array of B values T_b >= 0, and sequence b occupies rows
+ * off_b .. off_b + m_b + T_b - 1 with off_b = sum_{b' < b} (m_b' + T_b').
+ * Several documents of different lengths packed into one call, each with its
+ * own R-SWA mask (as multi-page training packs documents into one 32K
+ * sequence, GeekNews "Unlimited OCR", training setup).  Sets t_b = T_b.
+ * Errors as rswa_prefill.
+ */
+RSWA_API int rswa_prefill_varlen(rswa_cache* cache, const void* Q,
+                                 const void* K, const void* V, void* O,
+                                 const int64_t* m_per_seq,
+                                 const int64_t* t_per_seq, void* stream);
 
 /*
  * Append output t_b's key and value for every sequence: k, v are [B][H][d].
@@ -210,8 +242,9 @@ RSWA_API int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
                                            void* o, float* lse, void* stream);
 
 /*
- * Live cache size of sequence b in bytes: C(t_b) * H * d * 2 (K and V) *
- * element size, with C(t) = m_b + min(n, t) ("Unlimited-OCR deep dive",
+ * Live cache size of sequence b in bytes: C(t_b) * H_kv * d * 2 (K and V) *
+ * element size (H_kv = heads unless created with kv_heads), with
+ * C(t) = m_b + min(n, t) ("Unlimited-OCR deep dive",
  * cache-size line; GeekNews, KV cache management).  Synchronous: waits for
  * the device (cudaDeviceSynchronize) and reads m_b, t_b.  A test and
  * reporting helper, not a hot-path call.  Errors: RSWA_EINVAL, RSWA_ECUDA.
@@ -236,7 +269,7 @@ RSWA_API int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq,
 
 /*
  * Byte offsets of the K and V slabs inside the cache buffer.  Each slab is
- * [B][H][m + n][d] in the cache dtype: rows 0..m-1 of a (b, h) slab hold the
+ * [B][H_kv][m + n][d] in the cache dtype: rows 0..m-1 of a (b, h) slab hold the
  * prefix, rows m..m+n-1 the ring, output j in row m + (j mod n).  For
  * inspection and checkpointing; host-only, no CUDA call.
  * Errors: RSWA_EINVAL, RSWA_EHANDLE.

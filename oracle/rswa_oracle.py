@@ -32,7 +32,10 @@ R2  Prefix rows attend causally among themselves (the decoder is a causal LM
 R3  Softmax scale 1/sqrt(d); no bias, ALiBi or soft-cap.
 R4  Positions are absolute row indices of the concatenated [prefix | outputs]
     sequence; positional encodings are applied by the caller beforehand.
-R5  One KV head per query head (standard MHA).
+R5  One KV head per query head (standard MHA, the pages' baseline).  As an
+    extension beyond the pages, grouped heads (GQA) are supported: with H
+    query heads and H_kv key/value heads (H divisible by H_kv), query head h
+    reads KV head h // (H / H_kv).
 
 Notation: m = prefix length (L_m), n = output window, T = number of outputs,
 L = m + T rows.  Row i < m is a prefix row; row i >= m is output t = i - m.
@@ -60,6 +63,7 @@ __all__ = [
     "ring_outputs",
     "RingQueue",
     "attention_rows",
+    "kv_head",
     "prefill_attention",
     "prefill_cache",
     "append_kv",
@@ -194,19 +198,28 @@ def attention_rows(Q, K, V, m: int, n: int, rows=None):
     return O, lse
 
 
+def kv_head(h: int, H: int, Hkv: int) -> int:
+    """KV head read by query head h (R5)."""
+    return h // (H // Hkv)
+
+
 def prefill_attention(Q, K, V, m: int, n: int, rows=None):
-    """R-SWA prefill for token-major inputs Q, K, V of shape [L][H][d].
+    """R-SWA prefill for token-major inputs Q [L][H][d], K, V [L][H_kv][d].
 
     Returns (O [R][H][d], lse [R][H]) for the requested rows R (default all).
     """
     Q = np.asarray(Q, dtype=np.float64)
+    K = np.asarray(K)
+    V = np.asarray(V)
     L, H, d = Q.shape
+    Hkv = K.shape[1]
     rows = list(range(L)) if rows is None else list(rows)
-    O = np.empty((len(rows), H, np.shape(V)[2]), dtype=np.float64)
+    O = np.empty((len(rows), H, V.shape[2]), dtype=np.float64)
     lse = np.empty((len(rows), H), dtype=np.float64)
     for h in range(H):
-        O[:, h], lse[:, h] = attention_rows(Q[:, h], np.asarray(K)[:, h],
-                                            np.asarray(V)[:, h], m, n, rows)
+        g = kv_head(h, H, Hkv)
+        O[:, h], lse[:, h] = attention_rows(Q[:, h], K[:, g], V[:, g], m, n,
+                                            rows)
     return O, lse
 
 
@@ -218,7 +231,8 @@ def prefill_attention(Q, K, V, m: int, n: int, rows=None):
 def prefill_cache(K, V, m: int, n: int, T: int):
     """State after prefilling m prefix rows and T outputs of one sequence.
 
-    K, V: [m + T][H][d].  Returns dict(Kp, Vp [m][H][d], Kr, Vr [n][H][d] with
+    K, V: [m + T][H_kv][d].  Returns dict(Kp, Vp [m][H_kv][d], Kr, Vr
+    [n][H_kv][d] with
     never-written slots set to NaN, t = T).
     """
     K = np.asarray(K, dtype=np.float64)
@@ -233,7 +247,7 @@ def prefill_cache(K, V, m: int, n: int, T: int):
 
 
 def append_kv(state: dict, k, v, n: int) -> dict:
-    """Write output t's k, v ([H][d]) into slot t mod n, then t += 1."""
+    """Write output t's k, v ([H_kv][d]) into slot t mod n, then t += 1."""
     t = state["t"]
     Kr = state["Kr"].copy()
     Vr = state["Vr"].copy()
@@ -243,7 +257,8 @@ def append_kv(state: dict, k, v, n: int) -> dict:
 
 
 def decode_step(state: dict, q, n: int):
-    """Attend q ([H][d]) over the cache: the prefix plus the filled ring slots.
+    """Attend q ([H][d]) over the cache: the prefix plus the filled ring slots
+    (query head h reads KV head h // (H / H_kv)).
 
     The caller appends output t's k, v before decoding q_t, so the row attends
     to itself (R1).  Returns (o [H][d], lse [H]) in float64.
@@ -251,11 +266,13 @@ def decode_step(state: dict, q, n: int):
     q = np.asarray(q, dtype=np.float64)
     filled = sorted(ring_outputs(state["t"], n).keys())
     H = q.shape[0]
-    o = np.empty((H, state["Vp"].shape[2]), dtype=np.float64)
+    Hkv = state["Kr"].shape[1]
+    o = np.empty((H, state["Vr"].shape[2]), dtype=np.float64)
     lse = np.empty(H, dtype=np.float64)
     for h in range(H):
-        Kc = np.concatenate([state["Kp"][:, h], state["Kr"][filled, h]])
-        Vc = np.concatenate([state["Vp"][:, h], state["Vr"][filled, h]])
+        g = kv_head(h, H, Hkv)
+        Kc = np.concatenate([state["Kp"][:, g], state["Kr"][filled, g]])
+        Vc = np.concatenate([state["Vp"][:, g], state["Vr"][filled, g]])
         o[h], lse[h] = _attend(q[h], Kc, Vc)
     return o, lse
 

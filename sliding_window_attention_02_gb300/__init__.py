@@ -19,6 +19,7 @@ __all__ = [
     "RswaError", "load", "library_path", "declared_symbols",
     "RSWA_F32", "RSWA_BF16",
     "rswa_strerror", "rswa_cache_footprint", "rswa_cache_create",
+    "rswa_cache_footprint_gqa", "rswa_cache_create_gqa", "rswa_prefill_varlen",
     "rswa_cache_destroy", "rswa_prefill", "rswa_append_kv",
     "rswa_decode_step", "rswa_decode_step_fused",
     "rswa_decode_step_fused_static", "rswa_decode_block", "rswa_cache_bytes",
@@ -44,6 +45,14 @@ _SIGNATURES = {
     "rswa_cache_create": (_c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int,
                                    _c_int, _c_vp, _c_size,
                                    ctypes.POINTER(_c_vp)]),
+    "rswa_cache_footprint_gqa": (_c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int,
+                                          _c_int, _c_int, ctypes.POINTER(_c_size)]),
+    "rswa_cache_create_gqa": (_c_int, [_c_i64, _c_i64, _c_int, _c_int, _c_int,
+                                       _c_int, _c_int, _c_vp, _c_size,
+                                       ctypes.POINTER(_c_vp)]),
+    "rswa_prefill_varlen": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                     ctypes.POINTER(_c_i64), ctypes.POINTER(_c_i64),
+                                     _c_vp]),
     "rswa_cache_destroy": (_c_int, [_c_vp]),
     "rswa_prefill": (_c_int, [_c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
                               ctypes.POINTER(_c_i64), _c_i64, _c_vp]),
@@ -153,6 +162,25 @@ def rswa_cache_create(m, n, heads, head_dim, batch, dtype, buf):
     return h.value
 
 
+def rswa_cache_footprint_gqa(m, n, heads, kv_heads, head_dim, batch,
+                             dtype) -> int:
+    out = _c_size(0)
+    _check(load().rswa_cache_footprint_gqa(m, n, heads, kv_heads, head_dim,
+                                           batch, dtype, ctypes.byref(out)),
+           "rswa_cache_footprint_gqa")
+    return out.value
+
+
+def rswa_cache_create_gqa(m, n, heads, kv_heads, head_dim, batch, dtype, buf):
+    h = _c_vp()
+    _check(load().rswa_cache_create_gqa(m, n, heads, kv_heads, head_dim, batch,
+                                        dtype, _ptr(buf),
+                                        buf.numel() * buf.element_size(),
+                                        ctypes.byref(h)),
+           "rswa_cache_create_gqa")
+    return h.value
+
+
 def rswa_cache_destroy(handle) -> None:
     _check(load().rswa_cache_destroy(handle), "rswa_cache_destroy")
 
@@ -162,6 +190,15 @@ def rswa_prefill(handle, Q, K, V, O, m_per_seq, T, stream=None) -> None:
     _check(load().rswa_prefill(handle, _ptr(Q), _ptr(K), _ptr(V), _ptr(O), arr,
                                int(T), _stream(stream)),
            "rswa_prefill")
+
+
+def rswa_prefill_varlen(handle, Q, K, V, O, m_per_seq, t_per_seq,
+                        stream=None) -> None:
+    marr = (_c_i64 * len(m_per_seq))(*[int(x) for x in m_per_seq])
+    tarr = (_c_i64 * len(t_per_seq))(*[int(x) for x in t_per_seq])
+    _check(load().rswa_prefill_varlen(handle, _ptr(Q), _ptr(K), _ptr(V),
+                                      _ptr(O), marr, tarr, _stream(stream)),
+           "rswa_prefill_varlen")
 
 
 def rswa_append_kv(handle, k, v, stream=None) -> None:
@@ -243,14 +280,17 @@ def rswa_sync_status(handle) -> int:
 class RswaCache:
     """A cache plus the torch-allocated device buffer that backs it."""
 
-    def __init__(self, m, n, heads, head_dim, batch, dtype, device="cuda"):
+    def __init__(self, m, n, heads, head_dim, batch, dtype, device="cuda",
+                 kv_heads=None):
         import torch
         self.m, self.n, self.heads, self.head_dim = m, n, heads, head_dim
+        self.kv_heads = heads if kv_heads is None else kv_heads
         self.batch, self.dtype = batch, dtype
-        nbytes = rswa_cache_footprint(m, n, heads, head_dim, batch, dtype)
+        nbytes = rswa_cache_footprint_gqa(m, n, heads, self.kv_heads, head_dim,
+                                          batch, dtype)
         self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
-        self.handle = rswa_cache_create(m, n, heads, head_dim, batch, dtype,
-                                        self.buf)
+        self.handle = rswa_cache_create_gqa(m, n, heads, self.kv_heads,
+                                            head_dim, batch, dtype, self.buf)
 
     def close(self):
         if self.handle is not None:
@@ -266,6 +306,10 @@ class RswaCache:
     # thin forwards
     def prefill(self, Q, K, V, O, m_per_seq, T, stream=None):
         rswa_prefill(self.handle, Q, K, V, O, m_per_seq, T, stream)
+
+    def prefill_varlen(self, Q, K, V, O, m_per_seq, t_per_seq, stream=None):
+        rswa_prefill_varlen(self.handle, Q, K, V, O, m_per_seq, t_per_seq,
+                            stream)
 
     def append_kv(self, k, v, stream=None):
         rswa_append_kv(self.handle, k, v, stream)
@@ -295,11 +339,11 @@ class RswaCache:
         return rswa_sync_status(self.handle)
 
     def slabs(self):
-        """(K, V) views of the cache slabs [B][H][m + n][d] (for tests)."""
+        """(K, V) views of the cache slabs [B][H_kv][m + n][d] (for tests)."""
         import torch
         tdt = torch.float32 if self.dtype == RSWA_F32 else torch.bfloat16
         elt = 4 if self.dtype == RSWA_F32 else 2
-        B, H, R, d = self.batch, self.heads, self.m + self.n, self.head_dim
+        B, H, R, d = self.batch, self.kv_heads, self.m + self.n, self.head_dim
         nb = B * H * R * d * elt
         ko, vo = rswa_cache_kv_offsets(self.handle)
         Kt = self.buf[ko:ko + nb].view(tdt).view(B, H, R, d)

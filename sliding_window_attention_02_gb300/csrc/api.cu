@@ -6,6 +6,7 @@
 #include <mutex>
 #include <new>
 #include <unordered_set>
+#include <vector>
 
 #include "rswa_internal.h"
 
@@ -69,11 +70,12 @@ struct Layout {
   int chunk, max_chunks;
 };
 
-int valid_shape(int64_t m, int64_t n, int heads, int head_dim, int batch,
-                int dtype) {
+int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
+                int batch, int dtype) {
   if (dtype != RSWA_F32 && dtype != RSWA_BF16) return RSWA_EDTYPE;
   if (head_dim != 64 && head_dim != 128) return RSWA_EDTYPE;
-  if (m < 0 || n < 1 || heads < 1 || batch < 1) return RSWA_EINVAL;
+  if (m < 0 || n < 1 || heads < 1 || kv_heads < 1 || batch < 1) return RSWA_EINVAL;
+  if (heads % kv_heads != 0) return RSWA_EINVAL;
   if (m > (int64_t(1) << 30) || n > (int64_t(1) << 30)) return RSWA_EINVAL;
   if (heads > 4096 || batch > (1 << 20)) return RSWA_EINVAL;
   return RSWA_OK;
@@ -106,8 +108,8 @@ int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
   return c;
 }
 
-Layout make_layout(int64_t m, int64_t n, int heads, int head_dim, int batch,
-                   int dtype) {
+Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
+                   int batch, int dtype) {
   Layout L{};
   const size_t elt = dtype == RSWA_F32 ? 4 : 2;
   L.chunk = choose_chunk(m, n, heads, batch);
@@ -120,9 +122,9 @@ Layout make_layout(int64_t m, int64_t n, int heads, int head_dim, int batch,
   const size_t state_end = off;
   (void)state_end;
   L.k_off = off;
-  off = align_up(off + elt * (size_t)batch * heads * (size_t)(m + n) * head_dim);
+  off = align_up(off + elt * (size_t)batch * kv_heads * (size_t)(m + n) * head_dim);
   L.v_off = off;
-  off = align_up(off + elt * (size_t)batch * heads * (size_t)(m + n) * head_dim);
+  off = align_up(off + elt * (size_t)batch * kv_heads * (size_t)(m + n) * head_dim);
   L.part_off = off;
   off = align_up(off + sizeof(float) * (size_t)batch * heads * L.max_chunks *
                            (head_dim + 2));
@@ -149,25 +151,39 @@ const char* rswa_strerror(int status) {
 
 void rswa_debug_fail_next_cuda(int count) { g_fail_next.store(count < 0 ? 0 : count); }
 
+int rswa_cache_footprint_gqa(int64_t m, int64_t n, int heads, int kv_heads,
+                             int head_dim, int batch, int dtype,
+                             size_t* out_bytes) {
+  if (!out_bytes) return RSWA_EINVAL;
+  const int st = valid_shape(m, n, heads, kv_heads, head_dim, batch, dtype);
+  if (st != RSWA_OK) return st;
+  *out_bytes = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype).total;
+  return RSWA_OK;
+}
+
 int rswa_cache_footprint(int64_t m, int64_t n, int heads, int head_dim,
                          int batch, int dtype, size_t* out_bytes) {
-  if (!out_bytes) return RSWA_EINVAL;
-  const int st = valid_shape(m, n, heads, head_dim, batch, dtype);
-  if (st != RSWA_OK) return st;
-  *out_bytes = make_layout(m, n, heads, head_dim, batch, dtype).total;
-  return RSWA_OK;
+  return rswa_cache_footprint_gqa(m, n, heads, heads, head_dim, batch, dtype,
+                                  out_bytes);
 }
 
 int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim, int batch,
                       int dtype, void* device_buf, size_t buf_bytes,
                       rswa_cache** out) {
+  return rswa_cache_create_gqa(m, n, heads, heads, head_dim, batch, dtype,
+                               device_buf, buf_bytes, out);
+}
+
+int rswa_cache_create_gqa(int64_t m, int64_t n, int heads, int kv_heads,
+                          int head_dim, int batch, int dtype, void* device_buf,
+                          size_t buf_bytes, rswa_cache** out) {
   if (!out) return RSWA_EINVAL;
   *out = nullptr;
-  const int st = valid_shape(m, n, heads, head_dim, batch, dtype);
+  const int st = valid_shape(m, n, heads, kv_heads, head_dim, batch, dtype);
   if (st != RSWA_OK) return st;
   if (!device_buf || (reinterpret_cast<uintptr_t>(device_buf) % kAlign) != 0)
     return RSWA_EINVAL;
-  const Layout L = make_layout(m, n, heads, head_dim, batch, dtype);
+  const Layout L = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype);
   if (buf_bytes < L.total) return RSWA_ECAPACITY;
   if (injected_failure()) return RSWA_ECUDA;
   int dev = 0;
@@ -186,6 +202,7 @@ int rswa_cache_create(int64_t m, int64_t n, int heads, int head_dim, int batch,
   cv.cnt_bh = reinterpret_cast<int32_t*>(base + L.cnt_bh_off);
   cv.B = batch;
   cv.H = heads;
+  cv.Hkv = kv_heads;
   cv.d = head_dim;
   cv.dtype = dtype;
   cv.m_cap = m;
@@ -220,19 +237,20 @@ int rswa_cache_destroy(rswa_cache* cache) {
   return RSWA_OK;
 }
 
-int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
-                 const void* V, void* O, const int64_t* m_per_seq, int64_t T,
-                 void* stream) {
+int rswa_prefill_varlen(rswa_cache* cache, const void* Q, const void* K,
+                        const void* V, void* O, const int64_t* m_per_seq,
+                        const int64_t* t_per_seq, void* stream) {
   if (!live(cache)) return RSWA_EHANDLE;
   const CacheView& cv = cache->cv;
-  if (!m_per_seq || T < 0 || T > (int64_t(1) << 40)) return RSWA_EINVAL;
+  if (!m_per_seq || !t_per_seq) return RSWA_EINVAL;
   int64_t total_rows = 0;
   for (int b = 0; b < cv.B; ++b) {
-    if (m_per_seq[b] < 0) return RSWA_EINVAL;
+    if (m_per_seq[b] < 0 || t_per_seq[b] < 0 || t_per_seq[b] > (int64_t(1) << 40))
+      return RSWA_EINVAL;
     if (m_per_seq[b] > cv.m_cap) return RSWA_ECAPACITY;
-    total_rows += m_per_seq[b] + T;
+    total_rows += m_per_seq[b] + t_per_seq[b];
   }
-  // With no rows at all (every m_b = 0 and T = 0) the tensors may be NULL.
+  // With no rows at all (every m_b = 0 and T_b = 0) the tensors may be NULL.
   if (total_rows > 0 && (!K || !V)) return RSWA_EINVAL;
   if (O && !Q) return RSWA_EINVAL;
   if (!aligned16(K) || !aligned16(V) || (Q && !aligned16(Q)) ||
@@ -248,17 +266,17 @@ int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
     SeqTable st{};
     st.seq0 = b0;
     st.nseq = std::min(kMaxSeqPerLaunch, cv.B - b0);
-    st.T = T;
     int64_t max_rows = 0, rows = 0;
     int32_t tiles = 0;
     st.tile_off[0] = 0;
     for (int i = 0; i < st.nseq; ++i) {
-      const int64_t mb = m_per_seq[b0 + i];
+      const int64_t mb = m_per_seq[b0 + i], tb = t_per_seq[b0 + i];
       st.m[i] = (int32_t)mb;
+      st.T[i] = tb;
       st.row_off[i] = row + rows;
-      rows += mb + T;
-      max_rows = std::max(max_rows, mb + std::min(cv.n, T));
-      tiles += (int32_t)((mb + T + 127) / 128);
+      rows += mb + tb;
+      max_rows = std::max(max_rows, mb + std::min(cv.n, tb));
+      tiles += (int32_t)((mb + tb + 127) / 128);
       st.tile_off[i + 1] = tiles;
     }
     cudaError_t e = launch_prefill_cache(cv, st, K, V, max_rows, s);
@@ -272,8 +290,17 @@ int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
     }
     row += rows;
   }
-  (void)total_rows;
   return RSWA_OK;
+}
+
+int rswa_prefill(rswa_cache* cache, const void* Q, const void* K,
+                 const void* V, void* O, const int64_t* m_per_seq, int64_t T,
+                 void* stream) {
+  if (!live(cache)) return RSWA_EHANDLE;
+  if (T < 0) return RSWA_EINVAL;
+  std::vector<int64_t> t_per_seq((size_t)cache->cv.B, T);
+  return rswa_prefill_varlen(cache, Q, K, V, O, m_per_seq, t_per_seq.data(),
+                             stream);
 }
 
 int rswa_append_kv(rswa_cache* cache, const void* k, const void* v,
@@ -384,7 +411,7 @@ int rswa_cache_bytes(rswa_cache* cache, int b, size_t* out) {
   const int st = rswa_cache_len(cache, b, &len);
   if (st != RSWA_OK) return st;
   const size_t elt = cache->cv.dtype == RSWA_F32 ? 4 : 2;
-  *out = (size_t)len * cache->cv.H * cache->cv.d * 2 * elt;
+  *out = (size_t)len * cache->cv.Hkv * cache->cv.d * 2 * elt;
   return RSWA_OK;
 }
 

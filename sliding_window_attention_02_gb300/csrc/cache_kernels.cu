@@ -20,13 +20,13 @@ prefill_cache_kernel(CacheView cv, SeqTable st, const T* __restrict__ K,
   const int sl = blockIdx.y;                // sequence within the launch
   const int b = st.seq0 + sl;
   const int64_t m_b = st.m[sl];
-  const int64_t T_ = st.T;
+  const int64_t T_ = st.T[sl];
   const int64_t keep = min(cv.n, T_);       // outputs kept in the ring
   if (blockIdx.x == 0) {
     if (threadIdx.x == 0) cv.m_dev[b] = (int32_t)m_b;
     for (int h = threadIdx.x; h < cv.H; h += blockDim.x) cv.t_dev[(size_t)b * cv.H + h] = T_;
   }
-  const int D = cv.d, H = cv.H;
+  const int D = cv.d, H = cv.Hkv;           // K and V carry the KV heads
   const int nv = D * (int)sizeof(T) / 16;   // 16-byte vectors per head row
   for (int rr = 0; rr < 4; ++rr) {
     const int64_t r = (int64_t)blockIdx.x * 4 + rr;
@@ -53,15 +53,15 @@ prefill_cache_kernel(CacheView cv, SeqTable st, const T* __restrict__ K,
   }
 }
 
-// One CTA per sequence: write k, v of every head to slot t_b mod n, then
-// t_b += 1 (after every thread has read t_b).
+// One CTA per sequence: write k, v of every KV head to slot t_b mod n, then
+// t_b += 1 for every query head (after every thread has read t_b).
 template <typename T>
 __global__ void __launch_bounds__(128)
 append_kernel(CacheView cv, const T* __restrict__ k, const T* __restrict__ v) {
   const int b = blockIdx.x;
   const int64_t t_b = cv.t_dev[(size_t)b * cv.H];
   const int64_t slot = t_b % cv.n;
-  const int D = cv.d, H = cv.H;
+  const int D = cv.d, H = cv.Hkv;           // k, v: [B][Hkv][d]
   const int nv = D * (int)sizeof(T) / 16;
   for (int i = threadIdx.x; i < 2 * H * nv; i += blockDim.x) {
     const int kv = i / (H * nv);
@@ -73,7 +73,8 @@ append_kernel(CacheView cv, const T* __restrict__ k, const T* __restrict__ v) {
     reinterpret_cast<uint4*>(out)[vi] = reinterpret_cast<const uint4*>(in)[vi];
   }
   __syncthreads();
-  for (int h = threadIdx.x; h < H; h += blockDim.x) cv.t_dev[(size_t)b * H + h] = t_b + 1;
+  for (int h = threadIdx.x; h < cv.H; h += blockDim.x)
+    cv.t_dev[(size_t)b * cv.H + h] = t_b + 1;
 }
 
 cudaError_t launch_prefill_cache(const CacheView& cv, const SeqTable& st,

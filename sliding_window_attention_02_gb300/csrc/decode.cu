@@ -38,11 +38,13 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   if (c >= nch) return;
   const size_t bh = (size_t)b * cv.H + h;
   const int64_t t_b = cv.t_dev[bh];
+  const int grp = cv.H / cv.Hkv;                  // query heads per KV head
+  const size_t bkv = (size_t)b * cv.Hkv + h / grp;
 
-  const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
-  const T* kn = FUSED ? knew + bh * D : nullptr;
-  const T* vn = FUSED ? vnew + bh * D : nullptr;
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
+  const T* kn = FUSED ? knew + bkv * D : nullptr;
+  const T* vn = FUSED ? vnew + bkv * D : nullptr;
 
   int64_t j0, j1, sub = -1;
   if (c < cp) {
@@ -56,12 +58,13 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     j1 = cv.m_cap + s1;
     if (FUSED) {
       const int64_t w = t_b % cv.n;  // slot of the new output
-      if (w >= s0 && w < s0 + chunk) {
-        sub = cv.m_cap + w;
-        // This CTA owns slot w: store the new k, v there.  No CTA of this
-        // launch reads slot w from the slab (it reads (knew, vnew) instead).
-        T* Kw = static_cast<T*>(cv.K) + (bh * cv.slab_rows + sub) * D;
-        T* Vw = static_cast<T*>(cv.V) + (bh * cv.slab_rows + sub) * D;
+      if (w >= s0 && w < s0 + chunk) sub = cv.m_cap + w;
+      if (sub >= 0 && h % grp == 0) {
+        // This CTA owns slot w for its KV head: store the new k, v there.
+        // No CTA of this launch reads slot w from the slab (it reads
+        // (knew, vnew) instead).
+        T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + sub) * D;
+        T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + sub) * D;
         constexpr int NV = D * sizeof(T) / 16;
         for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
           if (i < NV)
@@ -162,22 +165,24 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   const int h = blockIdx.x / CL, b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const size_t bh = (size_t)b * cv.H + h;
+  const int grp = cv.H / cv.Hkv;                  // query heads per KV head
+  const size_t bkv = (size_t)b * cv.Hkv + h / grp;
   griddep_wait();
   griddep_launch_dependents();
   const int64_t m_b = cv.m_dev[b];
   const int64_t t_b = cv.t_dev[bh];
-  const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
-  const T* kn = FUSED ? knew + bh * D : nullptr;
-  const T* vn = FUSED ? vnew + bh * D : nullptr;
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
+  const T* kn = FUSED ? knew + bkv * D : nullptr;
+  const T* vn = FUSED ? vnew + bkv * D : nullptr;
   const int64_t filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
   int64_t sub = -1;
   if (FUSED) {
     sub = cv.m_cap + t_b % cv.n;
-    if (rank == 0) {
+    if (rank == 0 && h % grp == 0) {
       // No CTA of this launch reads slot sub from the slab.
-      T* Kw = static_cast<T*>(cv.K) + (bh * cv.slab_rows + sub) * D;
-      T* Vw = static_cast<T*>(cv.V) + (bh * cv.slab_rows + sub) * D;
+      T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + sub) * D;
+      T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + sub) * D;
       constexpr int NV = D * sizeof(T) / 16;
       for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
         if (i < NV)

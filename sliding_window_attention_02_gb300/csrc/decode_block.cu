@@ -25,18 +25,20 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
   const int64_t i = qi / cv.H;
   const int h = (int)(qi % cv.H);
   const size_t bh = (size_t)b * cv.H + h;
+  const int kvh = h / (cv.H / cv.Hkv);
+  const size_t bkv = (size_t)b * cv.Hkv + kvh;
   const int64_t m_b = cv.m_dev[b];
   const int64_t t_b = cv.t_dev[bh];
   const int64_t n = cv.n;
-  const int64_t row_stride = (int64_t)cv.H * D;          // [B][k][H][D]
-  const size_t qrow = ((size_t)b * k + i) * cv.H + h;
+  const int64_t row_stride = (int64_t)cv.Hkv * D;        // k, v: [B][k][Hkv][D]
+  const size_t qrow = ((size_t)b * k + i) * cv.H + h;    // q, o: [B][k][H][D]
 
   float qf[C::EPL];
   load_q_frag<T, D>(q + qrow * D, lane, qf);
   SoftmaxState<C::EPL> st;
   st.init();
-  const T* Kb = static_cast<const T*>(cv.K) + bh * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bh * cv.slab_rows * D;
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
   // prefix
   attend_range<T, D>(qf, Kb, Vb, D, 0, m_b, 0, C::KEYS_WARP, -1, nullptr,
                      nullptr, lane, st);
@@ -54,8 +56,8 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
                          nullptr, nullptr, lane, st);
   }
   // block tokens 0..i (rows of the input, stride H*D)
-  const T* Kk = kblk + ((size_t)b * k * cv.H + h) * D;
-  const T* Vk = vblk + ((size_t)b * k * cv.H + h) * D;
+  const T* Kk = kblk + ((size_t)b * k * cv.Hkv + kvh) * D;
+  const T* Vk = vblk + ((size_t)b * k * cv.Hkv + kvh) * D;
   attend_range<T, D>(qf, Kk, Vk, row_stride, 0, i + 1, 0, C::KEYS_WARP, -1,
                      nullptr, nullptr, lane, st);
   merge_groups<T, D>(st);
@@ -70,14 +72,15 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
 }
 
 // One CTA per sequence: block token i -> ring slot (t_b + i) mod n for every
-// head, then t_b += k (after every thread has read t_b).
+// KV head, then t_b += k for every query head (after every thread has read
+// t_b).
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 append_block_kernel(CacheView cv, const T* __restrict__ kblk,
                     const T* __restrict__ vblk, int64_t k) {
   const int b = blockIdx.x;
-  const int H = cv.H;
-  const int64_t t_b = cv.t_dev[(size_t)b * H];
+  const int H = cv.Hkv;                          // k, v carry the KV heads
+  const int64_t t_b = cv.t_dev[(size_t)b * cv.H];
   constexpr int NV = D * sizeof(T) / 16;
   const int64_t total = 2 * k * H * NV;
   for (int64_t x = threadIdx.x; x < total; x += blockDim.x) {
@@ -93,7 +96,8 @@ append_block_kernel(CacheView cv, const T* __restrict__ kblk,
     reinterpret_cast<uint4*>(out)[vi] = reinterpret_cast<const uint4*>(in)[vi];
   }
   __syncthreads();
-  for (int h = threadIdx.x; h < H; h += blockDim.x) cv.t_dev[(size_t)b * H + h] = t_b + k;
+  for (int h = threadIdx.x; h < cv.H; h += blockDim.x)
+    cv.t_dev[(size_t)b * cv.H + h] = t_b + k;
 }
 
 template <typename T, int D>

@@ -26,18 +26,20 @@ prefill_rowwise_kernel(CacheView cv, SeqTable st, const T* __restrict__ Q,
   const int64_t i = grow - st.row_off[sl];           // row within sequence
   const int64_t m = st.m[sl];
   const int H = cv.H;
-  const int64_t stride = (int64_t)H * D;
-  const T* Kb = K + st.row_off[sl] * stride + (int64_t)h * D;
-  const T* Vb = V + st.row_off[sl] * stride + (int64_t)h * D;
+  const int64_t stride = (int64_t)H * D;          // Q, O: [rows][H][D]
+  const int64_t kstride = (int64_t)cv.Hkv * D;    // K, V: [rows][Hkv][D]
+  const int kvh = h / (H / cv.Hkv);
+  const T* Kb = K + st.row_off[sl] * kstride + (int64_t)kvh * D;
+  const T* Vb = V + st.row_off[sl] * kstride + (int64_t)kvh * D;
 
   float qf[C::EPL];
   load_q_frag<T, D>(Q + grow * stride + (int64_t)h * D, lane, qf);
   SoftmaxState<C::EPL> s;
   s.init();
-  attend_range<T, D>(qf, Kb, Vb, stride, 0, min(m, i + 1), 0, C::KEYS_WARP,
+  attend_range<T, D>(qf, Kb, Vb, kstride, 0, min(m, i + 1), 0, C::KEYS_WARP,
                      -1, nullptr, nullptr, lane, s);
   if (i >= m)
-    attend_range<T, D>(qf, Kb, Vb, stride, max(m, i - cv.n + 1), i + 1, 0,
+    attend_range<T, D>(qf, Kb, Vb, kstride, max(m, i - cv.n + 1), i + 1, 0,
                        C::KEYS_WARP, -1, nullptr, nullptr, lane, s);
   merge_groups<T, D>(s);
   if (lane < C::LPK) {

@@ -197,7 +197,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   const int pr = g - st.tile_off[sl];                      // pair in sequence
   const int m = st.m[sl];
   const int n = (int)min(cv.n, (int64_t)1 << 30);
-  const int L = m + (int)st.T;
+  const int L = m + (int)st.T[sl];
+  const int kvh = h / (H / cv.Hkv);                         // KV head read
   const int64_t row0 = st.row_off[sl];
   const int q0 = pr * 2 * BM;
   const TileRange tr = tile_range(q0, q0 + 2 * BM - 1, m, n, L);
@@ -225,7 +226,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int x0 = h * HD;
+      const int x0 = h * HD;                                 // Q column
+      const int xk = kvh * HD;                               // K, V column
       const int yq = (int)(row0 + q0);
       mbar_arrive_expect_tx(bar(B_Q), 2 * kTileB);
       tma_load_2d(sb + OFF_Q, &tmQ, x0, yq, bar(B_Q));
@@ -242,8 +244,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int y = (int)(row0 + (int64_t)tile_at(tr, idx >> 1) * BN);
         const uint32_t dst = sb + OFF_RING + s * kTileB;
         mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
-        tma_load_2d(dst, map, x0, y, bar(B_FULL + s));
-        tma_load_2d(dst + kSub, map, x0 + 64, y, bar(B_FULL + s));
+        tma_load_2d(dst, map, xk, y, bar(B_FULL + s));
+        tma_load_2d(dst + kSub, map, xk + 64, y, bar(B_FULL + s));
         ++issued;
       }
       // Drain: every copy issued has landed before the CTA may exit.
@@ -480,7 +482,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows][H*128] bf16 viewed as a 2-D tensor; box 64 columns x 128 rows,
+// [rows][heads*128] bf16 viewed as a 2-D tensor; box 64 columns x 128 rows,
 // 128-byte swizzle; rows past `rows` read as zero.
 bool make_map(CUtensorMap* map, const void* base, int H, int64_t rows) {
   EncodeTiledFn fn = encode_fn();
@@ -508,8 +510,8 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
   const int64_t end_row = st_in.row_off[0] + total_rows;
   if (end_row >= (int64_t(1) << 31)) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, Q, cv.H, end_row) || !make_map(&mk, K, cv.H, end_row) ||
-      !make_map(&mv, V, cv.H, end_row))
+  if (!make_map(&mq, Q, cv.H, end_row) || !make_map(&mk, K, cv.Hkv, end_row) ||
+      !make_map(&mv, V, cv.Hkv, end_row))
     return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
@@ -523,7 +525,7 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
   int pairs = 0;
   st.tile_off[0] = 0;
   for (int i = 0; i < st.nseq; ++i) {
-    const int64_t L = st.m[i] + st.T;
+    const int64_t L = st.m[i] + st.T[i];
     pairs += (int)((L + 2 * BM - 1) / (2 * BM));
     st.tile_off[i + 1] = pairs;
   }

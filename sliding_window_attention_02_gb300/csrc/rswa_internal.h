@@ -12,7 +12,9 @@ constexpr int kMaxSeqPerLaunch = 128;   // sequences per prefill launch
 constexpr int kDecodeThreads = 128;     // threads per decode CTA
 
 // Device view of a cache buffer.  All regions live in the caller's buffer.
-//   K, V    slabs [B][H][slab_rows][d], slab_rows = m_cap + n: rows
+// H query heads share Hkv key/value heads (H % Hkv == 0): query head h reads
+// KV head h / (H / Hkv); Hkv == H is standard multi-head attention.
+//   K, V    slabs [B][Hkv][slab_rows][d], slab_rows = m_cap + n: rows
 //           0..m_cap-1 are the prefix region, rows m_cap..m_cap+n-1 the ring.
 //   m_dev   int32 [B]     prefix length m_b
 //   t_dev   int64 [B][H]  outputs appended t_b, one copy per head so that a
@@ -30,7 +32,7 @@ struct CacheView {
   int32_t* err;
   float* part;
   int32_t* cnt_bh;
-  int B, H, d, dtype;
+  int B, H, Hkv, d, dtype;
   int64_t m_cap, n, slab_rows;
   int chunk;       // keys per decode CTA
   int max_chunks;  // ceil(m_cap / chunk) + ceil(n / chunk)
@@ -40,7 +42,7 @@ struct CacheView {
 struct SeqTable {
   int nseq;                              // sequences in this launch
   int seq0;                              // index of the first one
-  int64_t T;                             // outputs per sequence
+  int64_t T[kMaxSeqPerLaunch];           // outputs per sequence
   int64_t row_off[kMaxSeqPerLaunch];     // first row of each sequence
   int32_t m[kMaxSeqPerLaunch];           // prefix lengths
   int32_t tile_off[kMaxSeqPerLaunch + 1];// cumulative 128-row q-tiles

@@ -360,3 +360,130 @@ def test_errors_launch_nothing(cuda_lib):
     with pytest.raises(rswa.RswaError) as e:
         rswa.rswa_decode_step(h, K[:1], K[:1])
     assert e.value.status == 4
+
+
+# ---------------------------------------------------------------------------
+# grouped heads (H_kv < H) and varlen packed prefill
+# ---------------------------------------------------------------------------
+
+def _qkv_gqa(rows, H, Hkv, d, seed, dtype=torch.bfloat16):
+    Q = workloads.normal((rows, H, d), 3 * seed, 1.0, dtype)
+    K = workloads.normal((rows, Hkv, d), 3 * seed + 1, 1.0, dtype)
+    V = workloads.normal((rows, Hkv, d), 3 * seed + 2, 1.0, dtype)
+    return Q, K, V
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_gqa_prefill(cuda_lib, d):
+    rswa = cuda_lib
+    H, Hkv, n, T = 8, 2, 64, 150
+    m_list = [100, 260]
+    rows = sum(m + T for m in m_list)
+    Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=31)
+    cache = rswa.RswaCache(max(m_list), n, H, d, len(m_list), rswa.RSWA_BF16,
+                           kv_heads=Hkv)
+    O = torch.zeros_like(Q, device="cuda")
+    cache.prefill(Q.cuda(), K.cuda(), V.cuda(), O, m_list, T)
+    torch.cuda.synchronize()
+    off = 0
+    for b, m in enumerate(m_list):
+        L = m + T
+        ref, _ = oracle.prefill_attention(f64(Q[off:off + L]), f64(K[off:off + L]),
+                                          f64(V[off:off + L]), m, n)
+        assert_close(f64(O[off:off + L]), ref, 1, f"seq {b}")
+        assert cache.cache_bytes(b) == oracle.cache_len(m, n, T) * Hkv * d * 2 * 2
+        off += L
+
+
+@pytest.mark.parametrize("B,H,Hkv", [(1, 8, 2), (20, 8, 2), (2, 6, 3)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_gqa_decode(cuda_lib, B, H, Hkv, fused):
+    """B*H = 160 > 152 takes the split-K kernel, the others the cluster path."""
+    rswa = cuda_lib
+    d, n, T = 128, 16, 24
+    m_list = [40 + 23 * b for b in range(B)]
+    rows = sum(m + T for m in m_list)
+    Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=33)
+    offs = np.cumsum([0] + [m + T for m in m_list])
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, 0)
+    got = np.zeros((T, B, H, d))
+    for t in range(T):
+        r = [offs[b] + m_list[b] + t for b in range(B)]
+        q, k, v = (x[r].contiguous().cuda() for x in (Q, K, V))
+        o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+        if fused:
+            cache.decode_step_fused(q, k, v, o)
+        else:
+            cache.append_kv(k, v)
+            cache.decode_step(q, o)
+        got[t] = f64(o)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b, m in enumerate(m_list):
+        sl = slice(offs[b], offs[b] + m + T)
+        ref, _ = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n)
+        assert_close(got[:, b], ref[m:], 1, f"seq {b}")
+        assert cache.get_t(b) == T
+
+
+def test_gqa_decode_block(cuda_lib):
+    rswa = cuda_lib
+    B, H, Hkv, d, n = 2, 8, 4, 128, 32
+    m_list = [70, 130]
+    blocks = [7, 32, 1, 20]
+    T = sum(blocks)
+    rows = sum(m + T for m in m_list)
+    Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=35)
+    offs = np.cumsum([0] + [m + T for m in m_list])
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, 0)
+    refs = []
+    for b, m in enumerate(m_list):
+        sl = slice(offs[b], offs[b] + m + T)
+        refs.append(oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]),
+                                             m, n)[0])
+    t = 0
+    for kb in blocks:
+        r = [[offs[b] + m_list[b] + t + i for i in range(kb)] for b in range(B)]
+        q, k, v = (torch.stack([x[rr] for rr in r]).contiguous().cuda()
+                   for x in (Q, K, V))
+        o = torch.empty_like(q)
+        cache.decode_block(q, k, v, o)
+        torch.cuda.synchronize()
+        for b, m in enumerate(m_list):
+            assert_close(f64(o[b]), refs[b][m + t:m + t + kb], 1, f"t={t} seq {b}")
+        t += kb
+
+
+def test_varlen_prefill(cuda_lib):
+    """Documents of different prefix and output lengths packed in one call,
+    each with its own mask; the cache keeps each sequence's own ring."""
+    rswa = cuda_lib
+    H, d, n = 2, 128, 32
+    m_list, t_list = [50, 0, 300, 129], [10, 200, 0, 77]
+    rows = sum(m + t for m, t in zip(m_list, t_list))
+    Q, K, V = workloads.qkv(rows, H, d, 41, 1.0, torch.bfloat16)
+    cache = rswa.RswaCache(max(m_list), n, H, d, len(m_list), rswa.RSWA_BF16)
+    O = torch.zeros_like(Q, device="cuda")
+    cache.prefill_varlen(Q.cuda(), K.cuda(), V.cuda(), O, m_list, t_list)
+    torch.cuda.synchronize()
+    Ks, _ = cache.slabs()
+    off = 0
+    for b, (m, T) in enumerate(zip(m_list, t_list)):
+        L = m + T
+        ref, _ = oracle.prefill_attention(f64(Q[off:off + L]), f64(K[off:off + L]),
+                                          f64(V[off:off + L]), m, n)
+        assert_close(f64(O[off:off + L]), ref, 1, f"seq {b}")
+        assert cache.get_t(b) == T
+        assert cache.cache_len(b) == oracle.cache_len(m, n, T)
+        st = oracle.prefill_cache(f64(K[off:off + L]), f64(V[off:off + L]), m, n, T)
+        filled = sorted(oracle.ring_outputs(T, n))
+        np.testing.assert_array_equal(
+            f64(Ks[b, :, max(m_list):])[:, filled].transpose(1, 0, 2),
+            st["Kr"][filled])
+        off += L

@@ -245,9 +245,36 @@ def check_decode_equals_prefill_row(orc):
         np.testing.assert_array_equal(direct["Vr"][filled], state["Vr"][filled])
 
 
+def check_gqa_repeated_kv(orc):
+    """Grouped heads equal standard MHA with each KV head repeated for its
+    group of query heads (torch SDPA on explicitly repeated K, V)."""
+    rng = np.random.default_rng(6)
+    for (m, n, T, H, Hkv, d) in [(6, 4, 20, 4, 2, 8), (3, 2, 11, 6, 3, 16),
+                                 (5, 3, 9, 4, 1, 8)]:
+        L = m + T
+        sets = queue_simulation(m, n, L)
+        mask = np.zeros((L, L), dtype=bool)
+        for i, st in enumerate(sets):
+            mask[i, st] = True
+        Q = rng.standard_normal((L, H, d))
+        K = rng.standard_normal((L, Hkv, d))
+        V = rng.standard_normal((L, Hkv, d))
+        Kr = np.repeat(K, H // Hkv, axis=1)
+        Vr = np.repeat(V, H // Hkv, axis=1)
+        ref = _sdpa(Q, Kr, Vr, mask=mask)
+        got, _ = orc.prefill_attention(Q, K, V, m, n)
+        np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+        # and through the cache: decode step t equals prefill row m + t
+        state = orc.prefill_cache(K[:m], V[:m], m, n, 0)
+        for t in range(T):
+            state, o, _ = orc.decode_step_fused(state, Q[m + t], K[m + t],
+                                                V[m + t], n)
+            np.testing.assert_allclose(o, got[m + t], rtol=0, atol=1e-12)
+
+
 PINS = [check_mask_vs_queue, check_cache_size, check_ring, check_mask_golden,
         check_causal_sdpa, check_masked_sdpa, check_identity_values,
-        check_constant_v, check_decode_equals_prefill_row]
+        check_constant_v, check_decode_equals_prefill_row, check_gqa_repeated_kv]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
@@ -286,6 +313,7 @@ MUTATIONS = [
      "filled = sorted(ring_outputs(state[\"t\"] - 1, n).keys())"),
     ("values transposed", "return (w @ V) / s, mx + np.log(s)",
      "return (w @ V[:, ::-1]) / s, mx + np.log(s)"),
+    ("kv head modulo", "return h // (H // Hkv)", "return h % Hkv"),
 ]
 
 
