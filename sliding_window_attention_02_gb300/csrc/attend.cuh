@@ -16,12 +16,12 @@ namespace rswa {
 #define RSWA_DECODE_UNROLL 8
 #endif
 
-template <typename T, int D>
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
 struct AttendCfg {
   static constexpr int EPL = Elt<T>::kPerVec;
   static constexpr int LPK = D / EPL;
   static constexpr int KPW = 32 / LPK;
-  static constexpr int U = RSWA_DECODE_UNROLL;
+  static constexpr int U = UNROLL;
   static constexpr int KEYS_WARP = U * KPW;
   static_assert(D % EPL == 0 && 32 % LPK == 0, "unsupported head_dim");
 };
@@ -45,14 +45,14 @@ __device__ __forceinline__ void load_q_frag(const T* q_row, int lane,
 // table, e.g. the prefix rows and the ring slots of a cache slab).  This warp
 // takes the rows j_begin + first + it * step + (0 .. KEYS_WARP-1).  A row
 // whose physical index equals sub_row is read from (knew, vnew) instead.
-template <typename T, int D>
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
 __device__ __forceinline__ void attend_range(
     const float* qf, const T* __restrict__ Kb, const T* __restrict__ Vb,
     int64_t stride, int64_t j_begin, int64_t j_end, int64_t first,
     int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
     SoftmaxState<AttendCfg<T, D>::EPL>& st, int64_t seg_end = INT64_MAX,
     int64_t gap = 0) {
-  using C = AttendCfg<T, D>;
+  using C = AttendCfg<T, D, UNROLL>;
   constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
   const int grp = lane / LPK;
   const int col = (lane % LPK) * EPL;

@@ -147,6 +147,12 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
 }
 
 constexpr uint32_t kMaxClusterSize = 8;
+// Loads in flight per lane in the cluster path: 4 measured best on GB300 for
+// the latency-bound single-page step (the split-K path keeps 8).
+#ifndef RSWA_CLUSTER_UNROLL
+#define RSWA_CLUSTER_UNROLL 4
+#endif
+constexpr int kClusterUnroll = RSWA_CLUSTER_UNROLL;
 
 // Small-batch decode: a thread-block cluster of CL CTAs (NW warps each) per
 // (b, h).  The prefix rows and the filled ring slots form one logical key
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(NW * 32)
 decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
                       const T* __restrict__ knew, const T* __restrict__ vnew,
                       T* __restrict__ o, float* __restrict__ lse) {
-  using C = AttendCfg<T, D>;
+  using C = AttendCfg<T, D, kClusterUnroll>;
   const uint32_t rank = cluster_rank(), CL = cluster_size();
   const int h = blockIdx.x / CL, b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -202,7 +208,7 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   load_q_frag<T, D>(q + bh * D, lane, qf);
   SoftmaxState<C::EPL> st;
   st.init();
-  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
+  attend_range<T, D, kClusterUnroll>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
                      (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane, st, m_b,
                      cv.m_cap - m_b);
   merge_groups<T, D>(st);
@@ -271,7 +277,10 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   cluster_sync();                    // rank 0 done reading remote memory
 }
 
-constexpr int kClusterWarps = 8;
+#ifndef RSWA_CLUSTER_WARPS
+#define RSWA_CLUSTER_WARPS 8
+#endif
+constexpr int kClusterWarps = RSWA_CLUSTER_WARPS;
 constexpr int kMaxCluster = (int)kMaxClusterSize;
 
 // Launch with programmatic stream serialization so that a decode kernel may
@@ -306,7 +315,7 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, int cluster,
 static int64_t cluster_keys_per_iter(const CacheView& cv) {
   const int epl = cv.dtype == RSWA_F32 ? 4 : 8;
   const int kpw = 32 / (cv.d / epl);
-  return (int64_t)kClusterWarps * kpw * RSWA_DECODE_UNROLL;
+  return (int64_t)kClusterWarps * kpw * kClusterUnroll;
 }
 
 // Cluster size: enough CTAs for one iteration per CTA, at most 8.
