@@ -262,7 +262,9 @@ RSWA_API int rswa_cache_get_t(rswa_cache* cache, int b, int64_t* out);
  * Restore t_b for every sequence (t_per_seq: HOST array of B values >= 0),
  * e.g. when resuming a saved cache.  The ring is taken to hold outputs
  * t_b - min(n, t_b) .. t_b - 1 in slots j mod n; the call rewrites no
- * key/value data.  Errors: RSWA_EINVAL, RSWA_ECUDA.
+ * key/value data.  Copies from host memory and synchronises the stream
+ * before returning (not for use inside stream capture).
+ * Errors: RSWA_EINVAL, RSWA_ECUDA.
  */
 RSWA_API int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq,
                               void* stream);

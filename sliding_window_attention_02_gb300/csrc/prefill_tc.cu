@@ -468,17 +468,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // Looked up once (thread-safe static initialisation).
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -513,13 +512,10 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
   if (!make_map(&mq, Q, cv.H, end_row) || !make_map(&mk, K, cv.Hkv, end_row) ||
       !make_map(&mv, V, cv.Hkv, end_row))
     return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(
-        prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  // Per device (the attribute belongs to the current device's context).
+  cudaError_t e = cudaFuncSetAttribute(
+      prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   // Work units are pairs of 128-row tiles: tile_off counts pairs here.
   SeqTable st = st_in;
   int pairs = 0;
