@@ -214,6 +214,28 @@ def setup_batched(dev, seed=0):
             "steps": steps}
 
 
+def setup_batched_gqa(dev, seed=0):
+    """The batched-decode shape with 32 query heads over 8 KV heads."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["batched_decode_bf16"]
+    B, d, n, T = w.batch, w.head_dim, w.n, w.T
+    H, Hkv = 32, 8
+    m_list = workloads.prefix_lengths(B, *w.m_range, seed=seed)
+    rows = sum(m + T for m in m_list)
+    K = workloads.normal((rows, Hkv, d), 3 * seed + 1, 1.0, torch.bfloat16, dev)
+    V = workloads.normal((rows, Hkv, d), 3 * seed + 2, 1.0, torch.bfloat16, dev)
+    cache = rswa.RswaCache(w.m_range[1], n, H, d, B, rswa.RSWA_BF16, device=dev,
+                           kv_heads=Hkv)
+    cache.prefill(None, K, V, None, m_list, T)
+    q = workloads.normal((16 * B, H, d), 5000, 1.0, torch.bfloat16, dev)
+    k = workloads.normal((16 * B, Hkv, d), 5001, 1.0, torch.bfloat16, dev)
+    v = workloads.normal((16 * B, Hkv, d), 5002, 1.0, torch.bfloat16, dev)
+    return {"w": w, "H": H, "Hkv": Hkv, "cache": cache, "m_list": m_list,
+            "K": K, "V": V, "steps": (q, k, v)}
+
+
 def batched_step_bytes(m_list, w):
     B, H, d, n = w.batch, w.heads, w.head_dim, w.n
     keys = sum(m + n for m in m_list)
@@ -421,6 +443,29 @@ def run_extras(dev, peaks, quick=False):
         "l2": "inputs (%.2f GB) larger than L2" % (nbytes / 1e9),
         "timing": "%d fused steps per CUDA graph, events around replays" % GRAPH_STEPS}
     del bt
+    # batched decode with grouped heads (32 query / 8 KV heads) ------------
+    gq = setup_batched_gqa(dev)
+    H, Hkv = gq["H"], gq["Hkv"]
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    q, k, v = gq["steps"]
+    idx = [0]
+
+    def gstep():
+        i = idx[0] % 16
+        idx[0] += 1
+        gq["cache"].decode_step_fused(q[i * B:(i + 1) * B], k[i * B:(i + 1) * B],
+                                      v[i * B:(i + 1) * B], o, stream=s)
+    ms = graph_step_ms(gstep, s, GRAPH_STEPS, 3 if quick else 10)
+    # each KV head is read once per step; q, o per query head
+    nbytes = d * 2 * (2 * Hkv * sum(m + w.n for m in gq["m_list"]) +
+                      2 * B * H + 2 * B * Hkv)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["batched_decode_gqa"] = {
+        "workload": "B64 H32 (8 KV heads) d128 m~U{256..2048} n128 T4096 bf16, "
+                    "one fused step",
+        "us_per_step": round(ms * 1e3, 2), "algorithmic_bytes": nbytes,
+        "GB_per_s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    del gq
     # decode sweep ----------------------------------------------------------
     sw = setup_sweep(dev)
     w = sw["w"]

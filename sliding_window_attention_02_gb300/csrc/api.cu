@@ -90,7 +90,7 @@ int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
 // RSWA_DECODE_CTAS_PER_SM CTAs per SM.  Few heads: about 40 chunks per head,
 // 128..256 keys each (measured best on GB300 for one sequence with a 1K-10K
 // key cache; shorter caches take the cluster path).
-int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
+int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int batch) {
 #ifdef RSWA_DECODE_CHUNK
   return RSWA_DECODE_CHUNK;
 #endif
@@ -100,7 +100,10 @@ int choose_chunk(int64_t m, int64_t n, int heads, int batch) {
     while (c < want && c < 256) c <<= 1;
     return c;
   }
-  const int64_t keys = (int64_t)batch * heads * (m + n);
+  // one CTA per chunk of one K/V stream; a grouped kernel streams each KV
+  // head once per group of query heads
+  const int streams = heads / gqa_heads_per_cta(heads, kv_heads);
+  const int64_t keys = (int64_t)batch * streams * (m + n);
   const int64_t target = 152 * RSWA_DECODE_CTAS_PER_SM;
   int64_t want = (keys + target - 1) / target;
   int c = 64;
@@ -112,7 +115,7 @@ Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
                    int batch, int dtype) {
   Layout L{};
   const size_t elt = dtype == RSWA_F32 ? 4 : 2;
-  L.chunk = choose_chunk(m, n, heads, batch);
+  L.chunk = choose_chunk(m, n, heads, kv_heads, batch);
   L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
   size_t off = 0;
   L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);

@@ -131,3 +131,91 @@ __device__ __forceinline__ void merge_groups(SoftmaxState<AttendCfg<T, D>::EPL>&
 }
 
 }  // namespace rswa
+
+namespace rswa {
+
+// attend_range for G query heads that share one KV head: every K and V row
+// is loaded once and feeds G dot products and G softmax states.  qf holds
+// the G heads' fragments back to back (G * EPL floats).
+template <typename T, int D, int UNROLL, int G>
+__device__ __forceinline__ void attend_range_grouped(
+    const float* qf, const T* __restrict__ Kb, const T* __restrict__ Vb,
+    int64_t stride, int64_t j_begin, int64_t j_end, int64_t first,
+    int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
+    SoftmaxState<AttendCfg<T, D>::EPL>* st) {
+  using C = AttendCfg<T, D, UNROLL>;
+  constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
+  const int grp = lane / LPK;
+  const int col = (lane % LPK) * EPL;
+  for (int64_t base = j_begin + first; base < j_end; base += step) {
+    uint4 kr[U], vr[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = base + u * KPW + grp;
+      ok[u] = row < j_end;
+      const int64_t r = ok[u] ? row : j_begin;
+      const T* kp = Kb + r * stride + col;
+      const T* vp = Vb + r * stride + col;
+      if (r == sub_row) {
+        kp = knew + col;
+        vp = vnew + col;
+      }
+      kr[u] = ld_stream16(kp);
+      vr[u] = ld_stream16(vp);
+    }
+    float s[G][U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float kf[EPL];
+      Elt<T>::widen(kr[u], kf);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc = fmaf(qf[g * EPL + e], kf[e], acc);
+        s[g][u] = acc;
+      }
+    }
+#pragma unroll
+    for (int off = LPK / 2; off > 0; off >>= 1) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          s[g][u] += __shfl_xor_sync(0xffffffffu, s[g][u], off);
+    }
+    float p[G][U];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float mx = st[g].m;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (!ok[u]) s[g][u] = -INFINITY;
+        mx = fmaxf(mx, s[g][u]);
+      }
+      const float ref = (mx == -INFINITY) ? 0.f : mx;
+      const float alpha = fast_exp2(st[g].m - ref);
+      st[g].l *= alpha;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) st[g].acc[e] *= alpha;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        p[g][u] = fast_exp2(s[g][u] - ref);
+        st[g].l += p[g][u];
+      }
+      st[g].m = mx;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float vf[EPL];
+      Elt<T>::widen(vr[u], vf);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[g].acc[e] = fmaf(p[g][u], vf[e], st[g].acc[e]);
+    }
+  }
+}
+
+}  // namespace rswa

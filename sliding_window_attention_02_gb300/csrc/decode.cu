@@ -369,6 +369,8 @@ bool decode_use_small(const CacheView& cv) {
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           const void* v, void* o, float* lse, bool fused,
                           cudaStream_t s) {
+  if (cv.H != cv.Hkv && !decode_use_small(cv) && decode_gqa_heads_per_cta(cv) > 1)
+    return launch_decode_gqa(cv, q, k, v, o, lse, fused, s);
   if (cv.dtype == RSWA_F32) {
     if (cv.d == 64) return launch_decode_t<float, 64>(cv, q, k, v, o, lse, fused, s);
     return launch_decode_t<float, 128>(cv, q, k, v, o, lse, fused, s);

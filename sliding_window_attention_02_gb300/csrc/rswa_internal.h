@@ -57,6 +57,20 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
 cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
                          cudaStream_t s);
 bool decode_use_small(const CacheView& cv);
+// Grouped split-K decode (decode_gqa.cu): used for grouped caches whose query
+// heads per KV head are a multiple of 2 when the cluster path is not taken.
+// Query heads one CTA serves (4, 2, or 1 = not grouped); the chunk heuristic
+// counts the K/V streams this leaves, H / heads_per_cta per sequence.
+inline int gqa_heads_per_cta(int heads, int kv_heads) {
+  const int per_kv = heads / kv_heads;
+  if (per_kv % 4 == 0) return 4;
+  if (per_kv % 2 == 0) return 2;
+  return 1;
+}
+int decode_gqa_heads_per_cta(const CacheView& cv);
+cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
+                              const void* v, void* o, float* lse, bool fused,
+                              cudaStream_t s);
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
                                 const void* v, int64_t block, void* o, float* lse,
                                 cudaStream_t s);

@@ -395,13 +395,19 @@ def test_gqa_prefill(cuda_lib, d):
         off += L
 
 
-@pytest.mark.parametrize("B,H,Hkv", [(1, 8, 2), (20, 8, 2), (2, 6, 3)])
+@pytest.mark.parametrize("B,H,Hkv,m0", [
+    (1, 8, 2, 40),      # cluster path
+    (2, 6, 3, 40),      # cluster path
+    (20, 8, 2, 40),     # grouped split-K, 4 query heads per CTA
+    (20, 6, 3, 40),     # grouped split-K, 2 query heads per CTA
+    (26, 6, 1, 40),     # one KV head (multi-query), 2 per CTA
+    (1, 8, 2, 1500),    # few heads, long cache: grouped split-K
+])
 @pytest.mark.parametrize("fused", [False, True])
-def test_gqa_decode(cuda_lib, B, H, Hkv, fused):
-    """B*H = 160 > 152 takes the split-K kernel, the others the cluster path."""
+def test_gqa_decode(cuda_lib, B, H, Hkv, m0, fused):
     rswa = cuda_lib
     d, n, T = 128, 16, 24
-    m_list = [40 + 23 * b for b in range(B)]
+    m_list = [m0 + 23 * b for b in range(B)]
     rows = sum(m + T for m in m_list)
     Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=33)
     offs = np.cumsum([0] + [m + T for m in m_list])
