@@ -65,7 +65,8 @@ enum rswa_status {
   RSWA_EDTYPE = 3,    /* unsupported dtype / head_dim combination */
   RSWA_EHANDLE = 4,   /* NULL, destroyed or foreign handle */
   RSWA_ECUDA = 5,     /* a CUDA runtime call or launch failed */
-  RSWA_EDEVICE = 6    /* a kernel flagged an error (bounded wait ran out) */
+  RSWA_EDEVICE = 6    /* a kernel flagged an error (bounded wait ran out, or a
+                        launch shape that does not cover its work) */
 };
 
 enum rswa_dtype { RSWA_F32 = 0, RSWA_BF16 = 1 };

@@ -11,6 +11,7 @@
 // lse.  Per-step cost is m_b + min(n, t_b) keys: flat in t_b once t_b >= n
 // ("Unlimited OCR", GeekNews, kernel analysis).
 #include "attend.cuh"
+#include "tc_ptx.cuh"
 
 namespace rswa {
 
@@ -154,71 +155,152 @@ constexpr uint32_t kMaxClusterSize = 8;
 #endif
 constexpr int kClusterUnroll = RSWA_CLUSTER_UNROLL;
 
+// Bound on the cluster path's wait for the partials of its cluster.
+constexpr uint64_t kClusterWaitNs = 1000000000ull;
+
 // Small-batch decode: a thread-block cluster of CL CTAs (NW warps each) per
-// (b, h).  The prefix rows and the filled ring slots form one logical key
-// range, split evenly over the cluster; each CTA merges its warps in shared
-// memory, and CTA rank 0 combines the CL partials through distributed shared
-// memory between two cluster barriers - no global partials, no atomics.  Used
-// when few heads are in flight and every head's cache is short, where the
-// global split-K combine would only add latency.
+// (b, h).  The slab's physical rows 0 .. m_cap+n-1 are split evenly over the
+// cluster, one load per lane and row batch, so every K/V load is issued
+// straight after the dependency wait, beside the loads of m_b, t_b and q:
+// its address depends on none of them.  Rows outside the prefix [0, m_b)
+// and the filled ring slots are masked afterwards (score -inf, value 0: an
+// unfilled slot may hold any bits), and the ring slot this step appends to
+// is read from (knew, vnew).  Each CTA merges its warps in shared memory and
+// sends its partial to CTA rank 0 with asynchronous remote stores that
+// complete an mbarrier there; rank 0 waits on that barrier alone (bounded)
+// and combines the CL partials from its own shared memory while the other
+// CTAs have already exited - no global partials, no atomics, no remote loads
+// and no cluster barrier on the critical path.  Used when few heads are in
+// flight and every head's cache fits one row batch per CTA.
 template <typename T, int D, bool FUSED, int NW>
 __global__ void __launch_bounds__(NW * 32)
 decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
                       const T* __restrict__ knew, const T* __restrict__ vnew,
                       T* __restrict__ o, float* __restrict__ lse) {
   using C = AttendCfg<T, D, kClusterUnroll>;
+  constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
   const uint32_t rank = cluster_rank(), CL = cluster_size();
   const int h = blockIdx.x / CL, b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp_lane = lane / LPK;
+  const int col = (lane % LPK) * EPL;
   const size_t bh = (size_t)b * cv.H + h;
   const int grp = cv.H / cv.Hkv;                  // query heads per KV head
   const size_t bkv = (size_t)b * cv.Hkv + h / grp;
+  __shared__ float s_m[NW], s_l[NW];
+  __shared__ float s_acc[NW][D];
+  __shared__ float c_ml[kMaxClusterSize][2];   // rank 0's copy is the one used
+  __shared__ float c_acc[kMaxClusterSize][D];
+  __shared__ uint64_t c_bar;                   // rank 0: all partials landed
+  // One row batch of NW warps must cover a CTA's share of the slab (the
+  // host sizes the cluster so); the test is uniform over the cluster.
+  if ((cv.m_cap + cv.n + CL - 1) / CL > (int64_t)NW * C::KEYS_WARP) {
+    if (threadIdx.x == 0) flag_error(cv.err, kErrLaunchShape);
+    return;
+  }
+  if (rank == 0 && threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&c_bar), 1);
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&c_bar), CL * (D + 2) * 4);
+  }
+  // Publishes rank 0's barrier and marks this CTA as started; the matching
+  // wait precedes the first store into rank 0's shared memory.
+  cluster_arrive_release();
   griddep_wait();
   griddep_launch_dependents();
   const int64_t m_b = cv.m_dev[b];
   const int64_t t_b = cv.t_dev[bh];
+  float qf[EPL];
+  load_q_frag<T, D>(q + bh * D, lane, qf);
+  uint4 kn = make_uint4(0, 0, 0, 0), vn = kn;
+  if (FUSED) {
+    kn = ld_stream16(knew + bkv * D + col);
+    vn = ld_stream16(vnew + bkv * D + col);
+  }
+  // This CTA's physical rows [p0, p1); every lane's row of batch u.  A lane
+  // past p1 loads row R-1 and masks it.
+  const int64_t R = cv.m_cap + cv.n;
+  const int64_t per = (R + CL - 1) / CL;
+  const int64_t p0 = (int64_t)rank * per;
+  const int64_t p1 = min(R, p0 + per);
   const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
   const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
-  const T* kn = FUSED ? knew + bkv * D : nullptr;
-  const T* vn = FUSED ? vnew + bkv * D : nullptr;
+  uint4 kr[U], vr[U];
+  int64_t row[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    row[u] = p0 + (int64_t)warp * C::KEYS_WARP + u * KPW + grp_lane;
+    const int64_t r = row[u] < p1 ? row[u] : R - 1;
+    kr[u] = ld_stream16(Kb + r * D + col);
+    vr[u] = ld_stream16(Vb + r * D + col);
+  }
   const int64_t filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
-  int64_t sub = -1;
-  if (FUSED) {
-    sub = cv.m_cap + t_b % cv.n;
-    if (rank == 0 && h % grp == 0) {
-      // No CTA of this launch reads slot sub from the slab.
-      T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + sub) * D;
-      T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + sub) * D;
-      constexpr int NV = D * sizeof(T) / 16;
-      for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
-        if (i < NV)
-          reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(kn)[i];
-        else
-          reinterpret_cast<uint4*>(Vw)[i - NV] = reinterpret_cast<const uint4*>(vn)[i - NV];
-      }
+  const int64_t sub = FUSED ? cv.m_cap + t_b % cv.n : -1;
+  if (FUSED && rank == 0 && h % grp == 0) {
+    // Lanes that hold slot sub replace what they loaded with (knew, vnew),
+    // so the value this write races with is never used.
+    T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + sub) * D;
+    T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + sub) * D;
+    constexpr int NV = D * sizeof(T) / 16;
+    for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
+      if (i < NV)
+        reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(knew + bkv * D)[i];
+      else
+        reinterpret_cast<uint4*>(Vw)[i - NV] =
+            reinterpret_cast<const uint4*>(vnew + bkv * D)[i - NV];
     }
   }
-  // This CTA's share of the logical keys 0..m_b+filled-1 (0..m_b-1 ->
-  // prefix rows, m_b.. -> ring rows m_cap..).
-  const int64_t total = m_b + filled;
-  const int64_t per = (total + CL - 1) / CL;
-  const int64_t j0 = min(total, (int64_t)rank * per);
-  const int64_t j1 = min(total, j0 + per);
-  float qf[C::EPL];
-  load_q_frag<T, D>(q + bh * D, lane, qf);
-  SoftmaxState<C::EPL> st;
-  st.init();
-  attend_range<T, D, kClusterUnroll>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
-                     (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane, st, m_b,
-                     cv.m_cap - m_b);
-  merge_groups<T, D>(st);
-  __shared__ float s_m[NW], s_l[NW];
-  __shared__ float s_acc[NW][D];
-  __shared__ float p_ml[2];          // this CTA's partial, read by rank 0
-  __shared__ float p_acc[D];
-  if (lane < C::LPK) {
+  bool ok[U];
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) s_acc[warp][lane * C::EPL + e] = st.acc[e];
+  for (int u = 0; u < U; ++u) {
+    const int64_t p = row[u];
+    ok[u] = p < p1 && (p < m_b || (p >= cv.m_cap && p - cv.m_cap < filled));
+    if (p == sub) {
+      kr[u] = kn;
+      vr[u] = vn;
+    }
+    if (!ok[u]) vr[u] = make_uint4(0, 0, 0, 0);
+  }
+  float s[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float kf[EPL];
+    Elt<T>::widen(kr[u], kf);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+    s[u] = acc;
+  }
+#pragma unroll
+  for (int off = LPK / 2; off > 0; off >>= 1) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+  }
+  SoftmaxState<EPL> st;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (!ok[u]) s[u] = -INFINITY;
+    mx = fmaxf(mx, s[u]);
+  }
+  const float ref = (mx == -INFINITY) ? 0.f : mx;
+  st.m = mx;
+  st.l = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) st.acc[e] = 0.f;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float p = fast_exp2(s[u] - ref);
+    st.l += p;
+    float vf[EPL];
+    Elt<T>::widen(vr[u], vf);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) st.acc[e] = fmaf(p, vf[e], st.acc[e]);
+  }
+  merge_groups<T, D>(st);
+  if (lane < LPK) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) s_acc[warp][lane * EPL + e] = st.acc[e];
     if (lane == 0) {
       s_m[warp] = st.m;
       s_l[warp] = st.l;
@@ -226,55 +308,66 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   }
   __syncthreads();
   const int tid = threadIdx.x;
+  float A = 0.f, M = -INFINITY, Ls = 0.f;
   if (tid < D) {
-    float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
-    const float ref = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f, A = 0.f;
+    const float r0 = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float sc = fast_exp2(s_m[w] - ref);
+      const float sc = fast_exp2(s_m[w] - r0);
       Ls += s_l[w] * sc;
       A += s_acc[w][tid] * sc;
     }
-    p_acc[tid] = A;
+  }
+  cluster_wait();                    // rank 0's barrier is initialised
+  if (tid < D) {
+    const uint32_t bar = map_dsmem(&c_bar, 0);
+    st_async_f32(map_dsmem(&c_acc[rank][tid], 0), bar, A);
     if (tid == 0) {
-      p_ml[0] = M;
-      p_ml[1] = Ls;
+      st_async_f32(map_dsmem(&c_ml[rank][0], 0), bar, M);
+      st_async_f32(map_dsmem(&c_ml[rank][1], 0), bar, Ls);
     }
   }
-  cluster_sync();                    // partials of every CTA visible
-  if (rank == 0 && tid < D) {
-    float Mr[kMaxClusterSize], Lr[kMaxClusterSize], Ar[kMaxClusterSize];
-    float M = -INFINITY;
-#pragma unroll
-    for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
-      Mr[r] = -INFINITY;
-      Lr[r] = Ar[r] = 0.f;
-      if (r < CL) {
-        Mr[r] = ld_dsmem(&p_ml[0], r);
-        Lr[r] = ld_dsmem(&p_ml[1], r);
-        Ar[r] = ld_dsmem(&p_acc[tid], r);
+  if (rank != 0 || tid >= D) return;
+  // Bounded wait for the CL partials; gives up at once when an earlier
+  // launch on this cache already flagged an error.
+  const uint32_t bar = ptx::smem_u32(&c_bar);
+  if (!ptx::mbar_try_wait(bar, 0)) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t it = 1; !ptx::mbar_try_wait(bar, 0); ++it) {
+      if ((it & 63u) == 0 &&
+          (*(volatile int32_t*)cv.err != 0 ||
+           ptx::globaltimer_ns() - t0 > kClusterWaitNs)) {
+        flag_error(cv.err, kErrWaitTimeout);
+        return;
       }
-      M = fmaxf(M, Mr[r]);
-    }
-    const float ref = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f, A = 0.f;
-#pragma unroll
-    for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
-      const float sc = fast_exp2(Mr[r] - ref);
-      Ls += Lr[r] * sc;
-      A += Ar[r] * sc;
-    }
-    o[bh * D + tid] = (T)(Ls > 0.f ? A / Ls : 0.f);
-    if (tid == 0) {
-      if (lse) lse[bh] = Ls > 0.f ? (ref + log2f(Ls)) * kLn2 : -INFINITY;
-      // Every CTA of the cluster read t_b before the first cluster barrier.
-      if (FUSED) cv.t_dev[bh] = t_b + 1;
     }
   }
-  cluster_sync();                    // rank 0 done reading remote memory
+  float Mr[kMaxClusterSize], Lr[kMaxClusterSize], Ar[kMaxClusterSize];
+  float Mt = -INFINITY;
+#pragma unroll
+  for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
+    const bool in = r < CL;
+    Mr[r] = in ? c_ml[r][0] : -INFINITY;
+    Lr[r] = in ? c_ml[r][1] : 0.f;
+    Ar[r] = in ? c_acc[r][tid] : 0.f;
+    Mt = fmaxf(Mt, Mr[r]);
+  }
+  const float rt = (Mt == -INFINITY) ? 0.f : Mt;
+  float Lt = 0.f, At = 0.f;
+#pragma unroll
+  for (uint32_t r = 0; r < kMaxClusterSize; ++r) {
+    const float sc = fast_exp2(Mr[r] - rt);
+    Lt += Lr[r] * sc;
+    At += Ar[r] * sc;
+  }
+  o[bh * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
+  if (tid == 0) {
+    if (lse) lse[bh] = Lt > 0.f ? (rt + log2f(Lt)) * kLn2 : -INFINITY;
+    // Every CTA of the cluster read t_b before sending its partial.
+    if (FUSED) cv.t_dev[bh] = t_b + 1;
+  }
 }
 
 #ifndef RSWA_CLUSTER_WARPS
@@ -321,7 +414,11 @@ static int64_t cluster_keys_per_iter(const CacheView& cv) {
 // Cluster size: enough CTAs for one iteration per CTA, at most 8.
 static int cluster_size_for(const CacheView& cv) {
   const int64_t per = cluster_keys_per_iter(cv);
+#ifdef RSWA_CLUSTER_SIZE
+  const int64_t want = RSWA_CLUSTER_SIZE;
+#else
   const int64_t want = (cv.m_cap + cv.n + per - 1) / per;
+#endif
   return (int)(want < 1 ? 1 : (want > kMaxCluster ? kMaxCluster : want));
 }
 

@@ -17,6 +17,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 enum DeviceErr : int32_t {
   kErrNone = 0,
   kErrWaitTimeout = 1,
+  kErrLaunchShape = 2,   // a launch whose grid does not cover its work
 };
 
 __device__ __forceinline__ void flag_error(int32_t* err, int32_t code) {
@@ -41,10 +42,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Thread-block clusters: rank and size of this CTA's cluster, a full
-// cluster barrier (release/acquire: shared-memory writes before it are
-// visible to every CTA of the cluster after it), and a load from another
-// CTA's shared memory at the address of `p` in that CTA.
+// Thread-block clusters: rank and size of this CTA's cluster, the two halves
+// of the cluster barrier, and the cluster address of `p` in CTA `rank`.  An arrive with release semantics followed
+// by a wait with acquire semantics makes every shared-memory write issued
+// before the arrive (local or remote) visible to every CTA after the wait; a
+// relaxed arrive orders nothing and only marks this CTA as started.
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -55,18 +57,28 @@ __device__ __forceinline__ uint32_t cluster_size() {
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float ld_dsmem(const float* p, uint32_t rank) {
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_dsmem(const void* p, uint32_t rank) {
   const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  return remote;
+}
+// Asynchronous 4-byte store into another CTA's shared memory: `dst` and the
+// mbarrier `bar` are cluster addresses from map_dsmem; on arrival the store
+// completes 4 transaction bytes of that CTA's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t dst, uint32_t bar, float v) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+      :: "r"(dst), "r"(__float_as_uint(v)), "r"(bar) : "memory");
 }
 
 // 16-byte streaming load through the read-only path, no L1 allocation.
