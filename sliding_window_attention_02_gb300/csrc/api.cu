@@ -17,6 +17,10 @@ struct rswa_cache {
   int device;
   void* buf;
   size_t buf_bytes;
+  // False from creation and after every prefill or t restore until the next
+  // decode launch: the launch right after one of those must not read prefix
+  // rows or m_b before its dependency wait, later decode launches may.
+  std::atomic<bool> prefix_stable{false};
 };
 
 namespace {
@@ -265,6 +269,8 @@ int rswa_prefill_varlen(rswa_cache* cache, const void* Q, const void* K,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   int64_t row = 0;
+  // The next decode launch follows kernels that write the prefix and m_b.
+  cache->prefix_stable.store(false);
   for (int b0 = 0; b0 < cv.B; b0 += kMaxSeqPerLaunch) {
     SeqTable st{};
     st.seq0 = b0;
@@ -324,6 +330,7 @@ int rswa_decode_step(rswa_cache* cache, const void* q, void* o, float* lse,
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
   return status_of(launch_decode(cache->cv, q, nullptr, nullptr, o, lse, false,
+                                 cache->prefix_stable.exchange(true),
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -336,6 +343,7 @@ int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
   return status_of(launch_decode(cache->cv, q, k, v, o, lse, true,
+                                 cache->prefix_stable.exchange(true),
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -369,6 +377,7 @@ int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
   if (!g.ok) return RSWA_ECUDA;
   return status_of(launch_decode_fused_static(cache->cv, cache->device, q, k, v,
                                               o, lse,
+                                              cache->prefix_stable.exchange(true),
                                               static_cast<cudaStream_t>(stream)));
 }
 
@@ -427,6 +436,7 @@ int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq, void* stream) 
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cache->prefix_stable.store(false);
   if (launch_set_t(cache->cv, t_per_seq, s) != cudaSuccess) return RSWA_ECUDA;
   // The copy source is pageable host memory: finish before returning so the
   // caller may release it.

@@ -159,20 +159,23 @@ constexpr int kClusterUnroll = RSWA_CLUSTER_UNROLL;
 constexpr uint64_t kClusterWaitNs = 1000000000ull;
 
 // Small-batch decode: a thread-block cluster of CL CTAs (NW warps each) per
-// (b, h).  The slab's physical rows 0 .. m_cap+n-1 are split evenly over the
-// cluster, one load per lane and row batch, so every K/V load is issued
-// straight after the dependency wait, beside the loads of m_b, t_b and q:
-// its address depends on none of them.  Rows outside the prefix [0, m_b)
-// and the filled ring slots are masked afterwards (score -inf, value 0: an
-// unfilled slot may hold any bits), and the ring slot this step appends to
-// is read from (knew, vnew).  Each CTA merges its warps in shared memory and
-// sends its partial to CTA rank 0 with asynchronous remote stores that
-// complete an mbarrier there; rank 0 waits on that barrier alone (bounded)
-// and combines the CL partials from its own shared memory while the other
-// CTAs have already exited - no global partials, no atomics, no remote loads
-// and no cluster barrier on the critical path.  Used when few heads are in
-// flight and every head's cache fits one row batch per CTA.
-template <typename T, int D, bool FUSED, int NW>
+// (b, h).  Each CTA takes an even share of the slab's prefix rows
+// 0 .. m_cap-1 and of its ring rows m_cap .. m_cap+n-1, one load per lane
+// and row: these addresses depend on neither m_b nor t_b, so all loads are
+// issued at once.  With PREFETCH (the preceding kernel of the stream writes
+// no prefix row and no m_b of this cache) the prefix rows and m_b are even
+// loaded before the dependency wait, while the previous step drains; q, t_b,
+// the new k/v and the ring rows follow the wait.  Prefix rows at or past m_b
+// and ring slots not yet filled are masked (score -inf, value 0: such a row
+// may hold any bits), and the ring slot this step appends to is read from
+// (knew, vnew).  Each CTA merges its warps in shared memory and sends its
+// partial to CTA rank 0 with asynchronous remote stores that complete an
+// mbarrier there; rank 0 waits on that barrier alone (bounded) and combines
+// the CL partials from its own shared memory while the other CTAs have
+// already exited - no global partials, no atomics, no remote loads and no
+// cluster barrier on the critical path.  Used when few heads are in flight
+// and every head's cache fits one row batch per CTA.
+template <typename T, int D, bool FUSED, int NW, bool PREFETCH>
 __global__ void __launch_bounds__(NW * 32)
 decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
                       const T* __restrict__ knew, const T* __restrict__ vnew,
@@ -192,12 +195,32 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   __shared__ float c_ml[kMaxClusterSize][2];   // rank 0's copy is the one used
   __shared__ float c_acc[kMaxClusterSize][D];
   __shared__ uint64_t c_bar;                   // rank 0: all partials landed
-  // One row batch of NW warps must cover a CTA's share of the slab (the
-  // host sizes the cluster so); the test is uniform over the cluster.
-  if ((cv.m_cap + cv.n + CL - 1) / CL > (int64_t)NW * C::KEYS_WARP) {
+  // This CTA's prefix rows [a0, a1) and ring slots [r0, r1): local row
+  // i < np is prefix row a0 + i, then ring row m_cap + r0 + (i - np).
+  const int64_t pp = (cv.m_cap + CL - 1) / CL, pr = (cv.n + CL - 1) / CL;
+  // One row batch of NW warps must hold both shares (the host sizes the
+  // cluster so); the test is uniform over the cluster.
+  if (pp + pr > (int64_t)NW * C::KEYS_WARP) {
     if (threadIdx.x == 0) flag_error(cv.err, kErrLaunchShape);
     return;
   }
+  const int64_t a0 = min(cv.m_cap, (int64_t)rank * pp);
+  const int64_t a1 = min(cv.m_cap, a0 + pp);
+  const int64_t r0 = min(cv.n, (int64_t)rank * pr);
+  const int64_t r1 = min(cv.n, r0 + pr);
+  const int np = (int)(a1 - a0), nr = (int)(r1 - r0);
+  int64_t row[U];
+  int kind[U];                                  // 0 none, 1 prefix, 2 ring
+  uint4 kr[U], vr[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int i = warp * C::KEYS_WARP + u * KPW + grp_lane;
+    kind[u] = i < np ? 1 : (i < np + nr ? 2 : 0);
+    row[u] = kind[u] == 1 ? a0 + i : cv.m_cap + r0 + (i - np);
+    kr[u] = vr[u] = make_uint4(0, 0, 0, 0);
+  }
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
   if (rank == 0 && threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_u32(&c_bar), 1);
     ptx::fence_mbar_init();
@@ -206,9 +229,27 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   // Publishes rank 0's barrier and marks this CTA as started; the matching
   // wait precedes the first store into rank 0's shared memory.
   cluster_arrive_release();
+  int64_t m_b = 0;
+  if (PREFETCH) {
+    m_b = cv.m_dev[b];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (kind[u] == 1) {
+        kr[u] = ld_stream16(Kb + row[u] * D + col);
+        vr[u] = ld_stream16(Vb + row[u] * D + col);
+      }
+  }
   griddep_wait();
   griddep_launch_dependents();
-  const int64_t m_b = cv.m_dev[b];
+  if (!PREFETCH) {
+    m_b = cv.m_dev[b];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (kind[u] == 1) {
+        kr[u] = ld_stream16(Kb + row[u] * D + col);
+        vr[u] = ld_stream16(Vb + row[u] * D + col);
+      }
+  }
   const int64_t t_b = cv.t_dev[bh];
   float qf[EPL];
   load_q_frag<T, D>(q + bh * D, lane, qf);
@@ -217,23 +258,12 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
     kn = ld_stream16(knew + bkv * D + col);
     vn = ld_stream16(vnew + bkv * D + col);
   }
-  // This CTA's physical rows [p0, p1); every lane's row of batch u.  A lane
-  // past p1 loads row R-1 and masks it.
-  const int64_t R = cv.m_cap + cv.n;
-  const int64_t per = (R + CL - 1) / CL;
-  const int64_t p0 = (int64_t)rank * per;
-  const int64_t p1 = min(R, p0 + per);
-  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
-  uint4 kr[U], vr[U];
-  int64_t row[U];
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    row[u] = p0 + (int64_t)warp * C::KEYS_WARP + u * KPW + grp_lane;
-    const int64_t r = row[u] < p1 ? row[u] : R - 1;
-    kr[u] = ld_stream16(Kb + r * D + col);
-    vr[u] = ld_stream16(Vb + r * D + col);
-  }
+  for (int u = 0; u < U; ++u)
+    if (kind[u] == 2) {
+      kr[u] = ld_stream16(Kb + row[u] * D + col);
+      vr[u] = ld_stream16(Vb + row[u] * D + col);
+    }
   const int64_t filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
   const int64_t sub = FUSED ? cv.m_cap + t_b % cv.n : -1;
   if (FUSED && rank == 0 && h % grp == 0) {
@@ -253,9 +283,9 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   bool ok[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const int64_t p = row[u];
-    ok[u] = p < p1 && (p < m_b || (p >= cv.m_cap && p - cv.m_cap < filled));
-    if (p == sub) {
+    ok[u] = kind[u] == 1 ? row[u] < m_b
+                         : (kind[u] == 2 && row[u] - cv.m_cap < filled);
+    if (kind[u] == 2 && row[u] == sub) {
       kr[u] = kn;
       vr[u] = vn;
     }
@@ -312,10 +342,10 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
   if (tid < D) {
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
-    const float r0 = (M == -INFINITY) ? 0.f : M;
+    const float r0f = (M == -INFINITY) ? 0.f : M;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-      const float sc = fast_exp2(s_m[w] - r0);
+      const float sc = fast_exp2(s_m[w] - r0f);
       Ls += s_l[w] * sc;
       A += s_acc[w][tid] * sc;
     }
@@ -411,36 +441,48 @@ static int64_t cluster_keys_per_iter(const CacheView& cv) {
   return (int64_t)kClusterWarps * kpw * kClusterUnroll;
 }
 
-// Cluster size: enough CTAs for one iteration per CTA, at most 8.
+// Cluster size: the fewest CTAs (at most 8) whose share of the prefix rows
+// plus share of the ring rows fits one row batch of a CTA; kMaxCluster + 1
+// when none does.
 static int cluster_size_for(const CacheView& cv) {
-  const int64_t per = cluster_keys_per_iter(cv);
 #ifdef RSWA_CLUSTER_SIZE
-  const int64_t want = RSWA_CLUSTER_SIZE;
-#else
-  const int64_t want = (cv.m_cap + cv.n + per - 1) / per;
+  return RSWA_CLUSTER_SIZE;
 #endif
-  return (int)(want < 1 ? 1 : (want > kMaxCluster ? kMaxCluster : want));
+  const int64_t per = cluster_keys_per_iter(cv);
+  for (int c = 1; c <= kMaxCluster; ++c)
+    if ((cv.m_cap + c - 1) / c + (cv.n + c - 1) / c <= per) return c;
+  return kMaxCluster + 1;
+}
+
+template <typename T, int D, bool FUSED>
+static cudaError_t launch_cluster(const CacheView& cv, const T* q, const T* k,
+                                  const T* v, T* o, float* lse, bool prefetch,
+                                  cudaStream_t s) {
+  const int cl = cluster_size_for(cv);
+  const dim3 grid(cv.H * cl, cv.B), block(kClusterWarps * 32);
+  if (prefetch)
+    return launch_pdl(decode_cluster_kernel<T, D, FUSED, kClusterWarps, true>,
+                      grid, block, cl, s, cv, q, k, v, o, lse);
+  return launch_pdl(decode_cluster_kernel<T, D, FUSED, kClusterWarps, false>,
+                    grid, block, cl, s, cv, q, k, v, o, lse);
 }
 
 template <typename T, int D>
 static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
                                    const void* k, const void* v, void* o,
-                                   float* lse, bool fused, cudaStream_t s) {
+                                   float* lse, bool fused, bool prefetch,
+                                   cudaStream_t s) {
   const T* qq = (const T*)q;
   const T* kk = (const T*)k;
   const T* vv = (const T*)v;
   T* oo = (T*)o;
   cudaError_t e;
   if (decode_use_small(cv)) {
-    const int cl = cluster_size_for(cv);
-    dim3 grid(cv.H * cl, cv.B);
     if (fused)
-      e = launch_pdl(decode_cluster_kernel<T, D, true, kClusterWarps>, grid,
-                     dim3(kClusterWarps * 32), cl, s, cv, qq, kk, vv, oo, lse);
+      e = launch_cluster<T, D, true>(cv, qq, kk, vv, oo, lse, prefetch, s);
     else
-      e = launch_pdl(decode_cluster_kernel<T, D, false, kClusterWarps>, grid,
-                     dim3(kClusterWarps * 32), cl, s, cv, qq, (const T*)nullptr,
-                     (const T*)nullptr, oo, lse);
+      e = launch_cluster<T, D, false>(cv, qq, nullptr, nullptr, oo, lse,
+                                      prefetch, s);
   } else {
     dim3 grid(cv.max_chunks, cv.H, cv.B);
     if (fused)
@@ -454,27 +496,28 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
   return cudaGetLastError();
 }
 
-// The cluster path when every head's cache fits one iteration of a cluster
-// of at most 8 CTAs (two for wider clusters' worth of keys is the split-K
-// path's job) and all clusters fit in one wave of the 152 SMs.
+// The cluster path when every head's cache fits one row batch per CTA of a
+// cluster of at most 8 (longer caches are the split-K path's job) and all
+// clusters fit in one wave of the 152 SMs.
 bool decode_use_small(const CacheView& cv) {
-  const int64_t per = cluster_keys_per_iter(cv);
-  return cv.m_cap + cv.n <= kMaxCluster * per &&
-         (int64_t)cv.B * cv.H * cluster_size_for(cv) <= 152 * 2;
+  const int cl = cluster_size_for(cv);
+  return cl <= kMaxCluster && (int64_t)cv.B * cv.H * cl <= 152 * 2;
 }
 
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           const void* v, void* o, float* lse, bool fused,
-                          cudaStream_t s) {
+                          bool prefetch_prefix, cudaStream_t s) {
+  const bool pf = prefetch_prefix;
   if (cv.H != cv.Hkv && !decode_use_small(cv) && decode_gqa_heads_per_cta(cv) > 1)
     return launch_decode_gqa(cv, q, k, v, o, lse, fused, s);
   if (cv.dtype == RSWA_F32) {
-    if (cv.d == 64) return launch_decode_t<float, 64>(cv, q, k, v, o, lse, fused, s);
-    return launch_decode_t<float, 128>(cv, q, k, v, o, lse, fused, s);
+    if (cv.d == 64)
+      return launch_decode_t<float, 64>(cv, q, k, v, o, lse, fused, pf, s);
+    return launch_decode_t<float, 128>(cv, q, k, v, o, lse, fused, pf, s);
   }
   if (cv.d == 64)
-    return launch_decode_t<__nv_bfloat16, 64>(cv, q, k, v, o, lse, fused, s);
-  return launch_decode_t<__nv_bfloat16, 128>(cv, q, k, v, o, lse, fused, s);
+    return launch_decode_t<__nv_bfloat16, 64>(cv, q, k, v, o, lse, fused, pf, s);
+  return launch_decode_t<__nv_bfloat16, 128>(cv, q, k, v, o, lse, fused, pf, s);
 }
 
 }  // namespace rswa

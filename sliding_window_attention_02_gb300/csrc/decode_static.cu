@@ -58,7 +58,7 @@ size_t static_scratch_capacity() { return kStaticScratchBytes; }
 cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
                                        const void* q, const void* k,
                                        const void* v, void* o, float* lse,
-                                       cudaStream_t s) {
+                                       bool prefetch_prefix, cudaStream_t s) {
   size_t part_bytes = 0, cnt_bytes = 0;
   if (static_scratch_need(cv, &part_bytes, &cnt_bytes) > kStaticScratchBytes)
     return cudaErrorInvalidValue;
@@ -71,7 +71,7 @@ cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
   sv.cnt_bh = reinterpret_cast<int32_t*>(b + part_bytes);
   e = cudaMemsetAsync(sv.cnt_bh, 0, cnt_bytes, s);
   if (e != cudaSuccess) return e;
-  return launch_decode(sv, q, k, v, o, lse, true, s);
+  return launch_decode(sv, q, k, v, o, lse, true, prefetch_prefix, s);
 }
 
 }  // namespace rswa

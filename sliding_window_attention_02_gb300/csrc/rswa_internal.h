@@ -74,9 +74,12 @@ cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
                                 const void* v, int64_t block, void* o, float* lse,
                                 cudaStream_t s);
+// prefetch_prefix: the preceding kernel of the stream writes no prefix row
+// and no m_b of this cache (every decode launch but the first after a
+// prefill); the cluster path then loads them before its dependency wait.
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           const void* v, void* o, float* lse, bool fused,
-                          cudaStream_t s);
+                          bool prefetch_prefix, cudaStream_t s);
 cudaError_t launch_prefill_rowwise(const CacheView& cv, const SeqTable& st,
                                    const void* Q, const void* K, const void* V,
                                    void* O, int64_t total_rows, cudaStream_t s);
@@ -96,6 +99,6 @@ size_t static_scratch_capacity();
 cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
                                        const void* q, const void* k,
                                        const void* v, void* o, float* lse,
-                                       cudaStream_t s);
+                                       bool prefetch_prefix, cudaStream_t s);
 
 }  // namespace rswa

@@ -215,6 +215,38 @@ def test_bf16_decode(cuda_lib, case, fused):
         assert cache.cache_len(b) == oracle.cache_len(m, n, T)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_reprefill_then_decode_sees_new_prefix(cuda_lib, fused):
+    """Decode launches after the first one may load the prefix before their
+    dependency wait; the first decode after a new prefill may not.  Prefill
+    prefix A, decode three steps, prefill a different prefix B into the same
+    cache and decode at once, all enqueued back to back on one stream: every
+    step after the second prefill must match the oracle on prefix B."""
+    rswa = cuda_lib
+    m, n, H, d, T = 288, 128, 10, 128, 4
+    cache = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16)
+    seqs = [make_seq([m], T, H, d, 1, seed=s) for s in (21, 22)]
+    outs = []
+    for Q, K, V in seqs:
+        Qc, Kc, Vc = Q.cuda(), K.cuda(), V.cuda()
+        cache.prefill(None, Kc[:m], Vc[:m], None, [m], 0)
+        o = torch.empty(T, 1, H, d, dtype=torch.bfloat16, device="cuda")
+        for t in range(T):
+            q, k, v = (x[m + t][None].contiguous() for x in (Qc, Kc, Vc))
+            if fused:
+                cache.decode_step_fused(q, k, v, o[t])
+            else:
+                cache.append_kv(k, v)
+                cache.decode_step(q, o[t])
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for (Q, K, V), o in zip(seqs, outs):
+        ref = oracle_prefill(Q, K, V, [m], T, n)[0][0][m:]
+        assert_close(f64(o[:, 0]), ref, 1, "after prefill")
+    assert cache.get_t(0) == T
+
+
 BLOCK_CASES = [
     # (m_list, n, T, block sizes in order, H, d)
     ([288], 128, 0, [5, 1, 34, 128, 7, 100], 2, 128),
