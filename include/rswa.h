@@ -177,6 +177,13 @@ RSWA_API int rswa_append_kv(rswa_cache* cache, const void* k, const void* v,
  * per-step cost depends on m_b + min(n, t_b) only, not on t_b (GeekNews,
  * kernel analysis: constant decode-step duration under R-SWA).
  * An empty cache yields o = 0 and lse = -inf.
+ * Ordering: decode kernels use programmatic dependent launch and may start
+ * while the preceding kernel of the stream still runs.  Every decode call
+ * except the first after rswa_prefill, rswa_prefill_varlen or
+ * rswa_cache_set_t on this cache may read the cache's prefix rows and m_b
+ * before that kernel has finished, so between two such calls the prefix
+ * rows are read-only: write them only through the prefill calls, or before
+ * rswa_cache_set_t (which synchronises its stream).
  * Errors: RSWA_EINVAL, RSWA_EHANDLE, RSWA_ECUDA.
  */
 RSWA_API int rswa_decode_step(rswa_cache* cache, const void* q, void* o,
@@ -274,7 +281,9 @@ RSWA_API int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq,
  * Byte offsets of the K and V slabs inside the cache buffer.  Each slab is
  * [B][H_kv][m + n][d] in the cache dtype: rows 0..m-1 of a (b, h) slab hold the
  * prefix, rows m..m+n-1 the ring, output j in row m + (j mod n).  For
- * inspection and checkpointing; host-only, no CUDA call.
+ * inspection and checkpointing; host-only, no CUDA call.  Prefix rows written
+ * here must be followed by rswa_cache_set_t before the next decode call (see
+ * the ordering rule of rswa_decode_step).
  * Errors: RSWA_EINVAL, RSWA_EHANDLE.
  */
 RSWA_API int rswa_cache_kv_offsets(rswa_cache* cache, size_t* k_offset,
