@@ -37,8 +37,9 @@ L2_FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "decode_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh"],
-    "decode_cluster_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh"],
+    "decode_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh", "tc_ptx.cuh"],
+    "decode_cluster_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh",
+                              "tc_ptx.cuh"],
     "prefill_tc_kernel": ["prefill_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
 }
 
