@@ -808,6 +808,15 @@ def main_only(args):
         def step():
             sp["g_prefill"].replay()
             sp["g_decode"].replay()
+    elif args.only == "gqa":
+        gq = setup_batched_gqa(dev)
+        w = gq["w"]
+        o = torch.empty(w.batch, gq["H"], w.head_dim, dtype=torch.bfloat16,
+                        device=dev)
+        q, k, v = (x[:w.batch] for x in gq["steps"])
+
+        def step():
+            gq["cache"].decode_step_fused(q, k, v, o, stream=s)
     elif args.only in ("batched", "sweep"):
         st = setup_batched(dev) if args.only == "batched" else setup_sweep(dev)
         w = st["w"]
@@ -858,7 +867,7 @@ def main():
     ap.add_argument("--cpu-worker", type=float, default=None)
     ap.add_argument("--cpu-max-steps", type=int, default=None)
     ap.add_argument("--only", default=None,
-                    choices=["single_page", "batched", "sweep", "prefill"],
+                    choices=["single_page", "batched", "sweep", "gqa", "prefill"],
                     help="run one workload warmup+steps times and print its "
                          "mean step time (for profiling)")
     ap.add_argument("--layers", type=int, default=None,

@@ -93,7 +93,8 @@ RSWA_API int rswa_cache_footprint(int64_t m, int64_t n, int heads,
  * Create a cache over the caller's device buffer (>= footprint bytes,
  * 256-byte aligned).  The buffer stays owned by the caller and must outlive
  * the handle.  Creation zeroes the per-sequence state (every sequence empty:
- * m_b = t_b = 0) with a synchronous memset on the current device.
+ * m_b = t_b = 0) and the key/value slabs with a synchronous memset on the
+ * current device.
  * Errors: RSWA_EINVAL (null/misaligned buffer, bad sizes), RSWA_ECAPACITY
  * (buffer too small), RSWA_EDTYPE, RSWA_ECUDA.
  */

@@ -94,10 +94,26 @@ int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
 // RSWA_DECODE_CTAS_PER_SM CTAs per SM.  Few heads: about 40 chunks per head,
 // 128..256 keys each (measured best on GB300 for one sequence with a 1K-10K
 // key cache; shorter caches take the cluster path).
-int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int batch) {
+#ifndef RSWA_TC_WAVES
+#define RSWA_TC_WAVES 4
+#endif
+
+int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
+                 int dtype, int batch) {
 #ifdef RSWA_DECODE_CHUNK
   return RSWA_DECODE_CHUNK;
 #endif
+  if (gqa_tc_shape(heads, kv_heads, head_dim, dtype)) {
+    // Tensor-core grouped decode: one CTA per chunk of a KV head, two
+    // resident per SM; chunks are whole 128-key tiles, sized for about
+    // RSWA_TC_WAVES waves of CTAs.
+    const int64_t keys = (int64_t)batch * kv_heads * (m + n);
+    const int64_t target = 152 * 2 * RSWA_TC_WAVES;
+    const int64_t want = (keys + target - 1) / target;
+    int c = 128;
+    while (c < want && c < 2048) c <<= 1;
+    return c;
+  }
   if ((int64_t)batch * heads <= 152) {
     const int64_t want = (m + n + 39) / 40;
     int c = 128;
@@ -119,7 +135,7 @@ Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
                    int batch, int dtype) {
   Layout L{};
   const size_t elt = dtype == RSWA_F32 ? 4 : 2;
-  L.chunk = choose_chunk(m, n, heads, kv_heads, batch);
+  L.chunk = choose_chunk(m, n, heads, kv_heads, head_dim, dtype, batch);
   L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
   size_t off = 0;
   L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);
@@ -220,8 +236,11 @@ int rswa_cache_create_gqa(int64_t m, int64_t n, int heads, int kv_heads,
   c->device = dev;
   c->buf = device_buf;
   c->buf_bytes = buf_bytes;
-  // Zero the state words (m_b, t_b, error flag, counters); K/V need no init.
-  cudaError_t e = cudaMemsetAsync(device_buf, 0, L.k_off, 0);
+  // Zero the state words (m_b, t_b, error flag, counters) and the K/V
+  // slabs: rows no prefill or append has written yet then hold zeros, and
+  // a tensor-core tile that reaches past the rows it attends (masked, p = 0)
+  // multiplies finite values only.
+  cudaError_t e = cudaMemsetAsync(device_buf, 0, L.part_off, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
   if (e != cudaSuccess) {
     delete c;

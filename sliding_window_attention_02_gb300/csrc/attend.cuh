@@ -218,4 +218,199 @@ __device__ __forceinline__ void attend_range_grouped(
   }
 }
 
+// attend_range for G query heads of one KV head with U = LPK / G rows per
+// lane group and iteration, so that the G * U partial dot products of a lane
+// group are exactly LPK values.  A butterfly reduce-scatter over the LPK
+// lanes (offsets LPK/2 .. 1, each level keeping the half of the values
+// named by the lane's bit at that offset) leaves lane pos of the group with
+// the full score of head pos / U and row pos % U: 15 shuffles for 16 scores
+// instead of 64, and one exp2 per lane.  Each lane then keeps the running
+// maximum of every head (identical in all lanes), the partial sum l of its
+// own (head, row) slot, and its EPL columns of every head's accumulator; the
+// probabilities reach all lanes by shuffle for the value update.  Dot
+// products and value updates use the packed f32x2 FMA.  On return st[g]
+// holds m, l (summed over the head's U lanes) and acc, as attend_range_grouped
+// leaves them.
+template <typename T, int D, int G>
+struct GroupedRsCfg {
+  static constexpr int EPL = Elt<T>::kPerVec;
+  static constexpr int LPK = D / EPL;
+  static constexpr int KPW = 32 / LPK;
+  static constexpr int U = LPK / G;
+  static constexpr int KEYS_WARP = U * KPW;
+  static constexpr bool kUsable = G * U == LPK && U >= 1 && U <= 8 && EPL % 2 == 0;
+};
+
+// Per-lane running state of the reduce-scatter loop: packed q pairs and
+// accumulators of the G heads, every head's running maximum (identical in
+// all lanes) and the maximum and partial sum of this lane's own head.
+template <typename T, int D, int G>
+struct GroupedRsState {
+  static constexpr int NP = GroupedRsCfg<T, D, G>::EPL / 2;
+  uint64_t q2[G][NP], a2[G][NP];
+  float m[G];
+  float m_own, l_own;
+
+  __device__ __forceinline__ void init(const float* qf) {
+    constexpr int EPL = GroupedRsCfg<T, D, G>::EPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        q2[g][i] = f2_pack(qf[g * EPL + 2 * i], qf[g * EPL + 2 * i + 1]);
+        a2[g][i] = 0;
+      }
+    }
+    m_own = -INFINITY;
+    l_own = 0.f;
+  }
+
+  // One batch: the lane group's U rows (kr, vr: this lane's 16-byte slices;
+  // ok[u]: row u is a key; a row that is not has its value taken as 0, so
+  // any bits may stand in kr/vr for it).  pos = lane % LPK.
+  __device__ __forceinline__ void step(const uint4* kr, uint4* vr,
+                                       const bool* ok, int pos) {
+    using C = GroupedRsCfg<T, D, G>;
+    constexpr int EPL = C::EPL, LPK = C::LPK, U = C::U;
+    const int my_u = pos % U;
+    float v[G * U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float kf[EPL];
+      Elt<T>::widen(kr[u], kf);
+      uint64_t k2[NP];
+#pragma unroll
+      for (int i = 0; i < NP; ++i) k2[i] = f2_pack(kf[2 * i], kf[2 * i + 1]);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        uint64_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < NP; ++i) acc = f2_fma(q2[g][i], k2[i], acc);
+        float lo, hi;
+        f2_unpack(acc, lo, hi);
+        v[g * U + u] = lo + hi;
+      }
+    }
+    // reduce-scatter: value index g*U+u ends in lane pos = g*U+u
+#pragma unroll
+    for (int o = LPK / 2, n = LPK; o > 0; o >>= 1, n >>= 1) {
+      const bool up = (pos & o) != 0;
+#pragma unroll
+      for (int j = 0; j < n / 2; ++j) {
+        const float send = up ? v[j] : v[j + n / 2];
+        const float keep = up ? v[j + n / 2] : v[j];
+        v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    bool ok_own = ok[0];
+#pragma unroll
+    for (int u = 1; u < U; ++u)
+      if (my_u == u) ok_own = ok[u];
+    const float s_own = ok_own ? v[0] : -INFINITY;
+    float mx_own = s_own;
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1)
+      mx_own = fmaxf(mx_own, __shfl_xor_sync(0xffffffffu, mx_own, o));
+    // every head's new maximum, in every lane; the accumulators are
+    // rescaled only when some head's maximum grew (alpha is exactly 1
+    // otherwise)
+    float mn[G];
+    bool grew = false;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      mn[g] = fmaxf(m[g], __shfl_sync(0xffffffffu, mx_own, g * U, LPK));
+      grew |= mn[g] > m[g];
+    }
+    if (__any_sync(0xffffffffu, grew)) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float ref = (mn[g] == -INFINITY) ? 0.f : mn[g];
+        const float alpha = fast_exp2(m[g] - ref);
+        const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) a2[g][i] = f2_mul(a2[g][i], al2);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) m[g] = mn[g];
+    const float mo = fmaxf(m_own, mx_own);
+    const float ref_own = (mo == -INFINITY) ? 0.f : mo;
+    const float alpha_own = fast_exp2(m_own - ref_own);
+    m_own = mo;
+    const float p_own = fast_exp2(s_own - ref_own);
+    l_own = l_own * alpha_own + p_own;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!ok[u]) vr[u] = make_uint4(0, 0, 0, 0);
+      float vf[EPL];
+      Elt<T>::widen(vr[u], vf);
+      uint64_t v2[NP];
+#pragma unroll
+      for (int i = 0; i < NP; ++i) v2[i] = f2_pack(vf[2 * i], vf[2 * i + 1]);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float p = __shfl_sync(0xffffffffu, p_own, g * U + u, LPK);
+        const uint64_t p2 = f2_pack(p, p);
+#pragma unroll
+        for (int i = 0; i < NP; ++i) a2[g][i] = f2_fma(p2, v2[i], a2[g][i]);
+      }
+    }
+  }
+
+  // st[g] = (m, l summed over the head's U lanes, this lane's acc columns).
+  __device__ __forceinline__ void finish(SoftmaxState<GroupedRsCfg<T, D, G>::EPL>* st) {
+    using C = GroupedRsCfg<T, D, G>;
+    constexpr int LPK = C::LPK, U = C::U;
+    float l_sum = l_own;
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1) l_sum += __shfl_xor_sync(0xffffffffu, l_sum, o);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      st[g].m = m[g];
+      st[g].l = __shfl_sync(0xffffffffu, l_sum, g * U, LPK);
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        f2_unpack(a2[g][i], st[g].acc[2 * i], st[g].acc[2 * i + 1]);
+    }
+  }
+};
+
+// The reduce-scatter loop over a contiguous range of rows read straight
+// from global memory (16-byte loads, U rows in flight per lane).
+template <typename T, int D, int G>
+__device__ __forceinline__ void attend_range_grouped_rs(
+    const float* qf, const T* __restrict__ Kb, const T* __restrict__ Vb,
+    int64_t stride, int64_t j_begin, int64_t j_end, int64_t first,
+    int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
+    SoftmaxState<AttendCfg<T, D>::EPL>* st) {
+  using C = GroupedRsCfg<T, D, G>;
+  constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
+  static_assert(C::kUsable, "reduce-scatter shape");
+  const int grp = lane / LPK, pos = lane % LPK;
+  const int col = pos * EPL;
+  GroupedRsState<T, D, G> rs;
+  rs.init(qf);
+  for (int64_t base = j_begin + first; base < j_end; base += step) {
+    uint4 kr[U], vr[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t row = base + u * KPW + grp;
+      ok[u] = row < j_end;
+      const int64_t r = ok[u] ? row : j_begin;
+      const T* kp = Kb + r * stride + col;
+      const T* vp = Vb + r * stride + col;
+      if (r == sub_row) {
+        kp = knew + col;
+        vp = vnew + col;
+      }
+      kr[u] = ld_stream16(kp);
+      vr[u] = ld_stream16(vp);
+    }
+    rs.step(kr, vr, ok, pos);
+  }
+  rs.finish(st);
+}
+
 }  // namespace rswa

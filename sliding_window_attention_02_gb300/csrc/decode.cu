@@ -496,6 +496,12 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
   return cudaGetLastError();
 }
 
+// 1: grouped caches of the tensor-core shape decode on the tensor cores;
+// 0: on the CUDA cores (decode_gqa.cu).
+#ifndef RSWA_GQA_TC
+#define RSWA_GQA_TC 1
+#endif
+
 // The cluster path when every head's cache fits one row batch per CTA of a
 // cluster of at most 8 (longer caches are the split-K path's job) and all
 // clusters fit in one wave of the 152 SMs.
@@ -508,8 +514,12 @@ cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           const void* v, void* o, float* lse, bool fused,
                           bool prefetch_prefix, cudaStream_t s) {
   const bool pf = prefetch_prefix;
-  if (cv.H != cv.Hkv && !decode_use_small(cv) && decode_gqa_heads_per_cta(cv) > 1)
-    return launch_decode_gqa(cv, q, k, v, o, lse, fused, s);
+  if (cv.H != cv.Hkv && !decode_use_small(cv)) {
+    if (RSWA_GQA_TC && gqa_tc_supported(cv))
+      return launch_decode_gqa_tc(cv, q, k, v, o, lse, fused, s);
+    if (decode_gqa_heads_per_cta(cv) > 1)
+      return launch_decode_gqa(cv, q, k, v, o, lse, fused, s);
+  }
   if (cv.dtype == RSWA_F32) {
     if (cv.d == 64)
       return launch_decode_t<float, 64>(cv, q, k, v, o, lse, fused, pf, s);

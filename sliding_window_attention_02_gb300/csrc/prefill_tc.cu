@@ -484,10 +484,17 @@ EncodeTiledFn encode_fn() {
 // [rows][heads*128] bf16 viewed as a 2-D tensor; box 64 columns x 128 rows,
 // 128-byte swizzle; rows past `rows` read as zero.
 bool make_map(CUtensorMap* map, const void* base, int H, int64_t rows) {
+  return make_tmap_rows_bf16(map, base, (uint64_t)H * HD, (uint64_t)rows);
+}
+
+}  // namespace
+
+bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
+                         uint64_t rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)H * HD, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)H * HD * 2};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {64, 128};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
@@ -495,8 +502,6 @@ bool make_map(CUtensorMap* map, const void* base, int H, int64_t rows) {
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 bool prefill_tc_supported(const CacheView& cv) {
   return cv.dtype == RSWA_BF16 && cv.d == HD && encode_fn() != nullptr;

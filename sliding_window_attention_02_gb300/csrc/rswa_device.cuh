@@ -81,6 +81,27 @@ __device__ __forceinline__ void st_async_f32(uint32_t dst, uint32_t bar, float v
       :: "r"(dst), "r"(__float_as_uint(v)), "r"(bar) : "memory");
 }
 
+// Two float32 values in one 64-bit register for the packed f32x2 arithmetic
+// of sm_100 and later: each half is rounded like the scalar instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // 16-byte streaming load through the read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;

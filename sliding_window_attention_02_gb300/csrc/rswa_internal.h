@@ -1,6 +1,7 @@
 // Internal declarations shared by the host API and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -68,6 +69,20 @@ inline int gqa_heads_per_cta(int heads, int kv_heads) {
   return 1;
 }
 int decode_gqa_heads_per_cta(const CacheView& cv);
+// Grouped decode on the tensor cores (decode_gqa_tc.cu): bf16, d 128, 2..16
+// query heads per KV head; one CTA serves every query head of its KV head.
+inline bool gqa_tc_shape(int heads, int kv_heads, int head_dim, int dtype) {
+  const int per_kv = heads / kv_heads;
+  return dtype == RSWA_BF16 && head_dim == 128 && per_kv >= 2 && per_kv <= 16;
+}
+bool gqa_tc_supported(const CacheView& cv);
+cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,
+                                 const void* k, const void* v, void* o,
+                                 float* lse, bool fused, cudaStream_t s);
+// [rows][cols] bf16, row-major, as a 2-D TMA map: box 64 columns x 128 rows,
+// 128-byte swizzle; rows past `rows` read as zero.
+bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
+                         uint64_t rows);
 cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
                               const void* v, void* o, float* lse, bool fused,
                               cudaStream_t s);

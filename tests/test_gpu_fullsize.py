@@ -78,6 +78,29 @@ def test_batched_decode_full(cuda_lib):
         assert bt["cache"].cache_len(b) == oracle.cache_len(m, n, T + 1)
 
 
+def test_batched_gqa_decode_full(cuda_lib):
+    """The batched GQA extra (B 64, H 32 over 8 KV heads, m ~ U{256..2048},
+    ring full) in bench.py's launch configuration, sampled sequences."""
+    dev = torch.device("cuda", 0)
+    gq = bench.setup_batched_gqa(dev)
+    w = gq["w"]
+    B, d, n, T, H = w.batch, w.head_dim, w.n, w.T, gq["H"]
+    q, k, v = (x[:B] for x in gq["steps"])
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, device=dev)
+    gq["cache"].decode_step_fused(q, k, v, o, lse)
+    torch.cuda.synchronize()
+    assert gq["cache"].sync_status() == 0
+    offs = np.cumsum([0] + [m + T for m in gq["m_list"]])
+    for b in [0, 7, 31, 63]:
+        m = gq["m_list"][b]
+        st = _seq_state(gq["K"], gq["V"], offs[b], m, n, T)
+        st, ro, rl = oracle.decode_step_fused(st, f64(q[b]), f64(k[b]), f64(v[b]), n)
+        check(f64(o[b]), ro, f"seq {b} (m={m})")
+        assert np.abs(f64(lse[b]) - rl).max() <= 1e-3
+        assert gq["cache"].get_t(b) == T + 1
+
+
 @pytest.mark.parametrize("T", [256, 100000])
 def test_sweep_decode_full(cuda_lib, T):
     dev = torch.device("cuda", 0)

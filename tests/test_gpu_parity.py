@@ -434,6 +434,7 @@ def test_gqa_prefill(cuda_lib, d):
     (20, 6, 3, 40),     # grouped split-K, 2 query heads per CTA
     (26, 6, 1, 40),     # one KV head (multi-query), 2 per CTA
     (1, 8, 2, 1500),    # few heads, long cache: grouped split-K
+    (1, 8, 2, 6000),    # 256-row chunks: each warp's stage ring wraps
 ])
 @pytest.mark.parametrize("fused", [False, True])
 def test_gqa_decode(cuda_lib, B, H, Hkv, m0, fused):
@@ -462,8 +463,92 @@ def test_gqa_decode(cuda_lib, B, H, Hkv, m0, fused):
     assert cache.sync_status() == 0
     for b, m in enumerate(m_list):
         sl = slice(offs[b], offs[b] + m + T)
-        ref, _ = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n)
-        assert_close(got[:, b], ref[m:], 1, f"seq {b}")
+        ref, _ = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n,
+                                          rows=list(range(m, m + T)))
+        assert_close(got[:, b], ref, 1, f"seq {b}")
+        assert cache.get_t(b) == T
+
+
+@pytest.mark.parametrize("dtype,d", [(1, 64), (0, 128), (0, 64)],
+                         ids=["bf16-d64", "f32-d128", "f32-d64"])
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (6, 3)], ids=["G4", "G2"])
+def test_gqa_decode_dtypes(cuda_lib, dtype, d, H, Hkv):
+    """Grouped split-K decode on the CUDA cores, for the element types and
+    head sizes the tensor-core kernel does not take: the reduce-scatter loop
+    wherever its shape fits, the plain grouped loop for float32 d 128 with
+    two heads per CTA."""
+    rswa = cuda_lib
+    B, n, T = 20, 16, 12
+    m_list = [300 + 37 * b for b in range(B)]
+    rows = sum(m + T for m in m_list)
+    Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=44, dtype=tdt(dtype))
+    offs = np.cumsum([0] + [m + T for m in m_list])
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, dtype, kv_heads=Hkv)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, 0)
+    got = np.zeros((T, B, H, d))
+    lse_got = np.zeros((T, B, H))
+    for t in range(T):
+        r = [offs[b] + m_list[b] + t for b in range(B)]
+        q, k, v = (x[r].contiguous().cuda() for x in (Q, K, V))
+        o = torch.empty(B, H, d, dtype=tdt(dtype), device="cuda")
+        lse = torch.empty(B, H, device="cuda")
+        cache.decode_step_fused(q, k, v, o, lse)
+        got[t] = f64(o)
+        lse_got[t] = f64(lse)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b, m in enumerate(m_list):
+        sl = slice(offs[b], offs[b] + m + T)
+        ref, rl = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n,
+                                           rows=list(range(m, m + T)))
+        assert_close(got[:, b], ref, dtype, f"seq {b}")
+        assert np.abs(lse_got[:, b] - rl).max() <= (1e-4 if dtype == 0 else 1e-3)
+        assert cache.get_t(b) == T
+
+
+def test_gqa_decode_tc_multitile(cuda_lib):
+    """Grouped decode with several 128-key tiles per split-K chunk (48
+    sequences x 8 KV heads of ~800 keys give 512-key chunks), so the K/V ring
+    wraps, S^T alternates buffers and PV(j-1) overlaps the softmax of tile j.
+    Keys planted late in a chunk (q-aligned, large) raise a head's running
+    maximum by far more than 2^8 after the first tile, which forces the O^T
+    rescale; the outputs must still match the oracle."""
+    rswa = cuda_lib
+    B, H, Hkv, d, n, T = 48, 32, 8, 128, 128, 3
+    per = H // Hkv
+    m_list = [700 + 11 * b for b in range(B)]
+    rows = sum(m + T for m in m_list)
+    Q, K, V = _qkv_gqa(rows, H, Hkv, d, seed=55)
+    offs = np.cumsum([0] + [m + T for m in m_list])
+    for b in range(0, B, 5):                # spikes in tiles 2 and 3 of chunk 0
+        for r, kvh in ((300 + b, b % Hkv), (450 + 2 * b, (b + 3) % Hkv)):
+            qv = Q[offs[b] + m_list[b], kvh * per].float()
+            K[offs[b] + r, kvh] = (qv / qv.norm() * 40.0).to(torch.bfloat16)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b]] for b in range(B)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, 0)
+    got = np.zeros((T, B, H, d))
+    lse_got = np.zeros((T, B, H))
+    for t in range(T):
+        r = [offs[b] + m_list[b] + t for b in range(B)]
+        q, k, v = (x[r].contiguous().cuda() for x in (Q, K, V))
+        o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, H, device="cuda")
+        cache.decode_step_fused(q, k, v, o, lse)
+        got[t] = f64(o)
+        lse_got[t] = f64(lse)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b in [0, 1, 5, 10, 23, 47]:
+        m = m_list[b]
+        sl = slice(offs[b], offs[b] + m + T)
+        ref, rl = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n,
+                                           rows=list(range(m, m + T)))
+        assert_close(got[:, b], ref, 1, f"seq {b}")
+        assert np.abs(lse_got[:, b] - rl).max() <= 1e-3
         assert cache.get_t(b) == T
 
 
