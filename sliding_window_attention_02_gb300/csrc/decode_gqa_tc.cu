@@ -65,7 +65,8 @@ constexpr int B_SFREE = B_S + 2;            // 2: S^T(j) read (128 arrivals)
 constexpr int B_P = B_SFREE + 2;            // 2: P^T(j) in smem (128 arrivals)
 constexpr int B_PFREE = B_P + 2;            // 2: PV(j) done
 constexpr int B_O = B_PFREE + 2;            // all MMAs done
-constexpr int NBAR = B_O + 1;
+constexpr int B_SYNC = B_O + 1;             // softmax warps' barrier (128)
+constexpr int NBAR = B_SYNC + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NBAR;    // tmem slot, flags
 constexpr uint32_t OFF_RED = OFF_MISC + 16;          // [2][4][16] + [4][16]
 constexpr uint32_t kSmemBytes = OFF_RED + (2 * 4 * NQ + 4 * NQ) * 4 + 1024;
@@ -74,10 +75,6 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
-
-__device__ __forceinline__ void softmax_bar() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 
 // Byte offset of element (row r, column c) in a K-major bf16 operand made of
 // 64-column atoms of `atom` bytes, 128-byte swizzle (16-byte chunk index
@@ -115,7 +112,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 
   if (tid == 0) {
     for (int k = 0; k < NBAR; ++k)
-      mbar_init(bar(k), (k >= B_SFREE && k < B_PFREE) ? 128u : 1u);
+      mbar_init(bar(k), ((k >= B_SFREE && k < B_PFREE) || k == B_SYNC) ? 128u : 1u);
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
@@ -286,8 +283,22 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Waits agreed by the whole warp (lanes stay converged for the
+    // warp-collective TMEM loads and shuffles), and a barrier over the four
+    // softmax warps on an mbarrier: bounded, so a warp that gives up cannot
+    // leave the others blocked.
+    auto wait_all = [&](int k, uint32_t parity) {
+      return __all_sync(0xffffffffu, mbar_wait(bar(k), parity, abort_flag, kWaitLimitNs));
+    };
+    int n_sync = 0;
+    auto soft_sync = [&]() {
+      mbar_arrive(bar(B_SYNC));
+      const bool r = mbar_wait(bar(B_SYNC), n_sync & 1, abort_flag, kWaitLimitNs);
+      ++n_sync;
+      return __all_sync(0xffffffffu, r);
+    };
     for (int j = 0; live && j < nt; ++j) {
-      if (!mbar_wait(bar(B_S + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs)) break;
+      if (!wait_all(B_S + (j & 1), (j >> 1) & 1)) break;
       tc_fence_after();
       uint32_t r[16];
       tmem_ld16(tmem + lane_off + TM_S + 16 * (j & 1), r);
@@ -309,7 +320,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
           v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
         if (lane == 0) rm[warp * NQ + g] = v;
       }
-      softmax_bar();
+      if (!soft_sync()) break;
       bool grow = false;
       float mt[G];
 #pragma unroll
@@ -330,9 +341,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
           l_t[g] *= alpha[g];
         }
         if (j >= 1) {
-          if (!mbar_wait(bar(B_PFREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort_flag,
-                         kWaitLimitNs))
-            break;
+          if (!wait_all(B_PFREE + ((j - 1) & 1), ((j - 1) >> 1) & 1)) break;
           tc_fence_after();
           uint32_t ov[16];
           tmem_ld16(tmem + lane_off + TM_O, ov);
@@ -345,9 +354,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         }
       }
       // P^T(j): buffer j & 1 is free once PV(j-2) has completed.
-      if (j >= 2 && !mbar_wait(bar(B_PFREE + (j & 1)), ((j - 2) >> 1) & 1, abort_flag,
-                               kWaitLimitNs))
-        break;
+      if (j >= 2 && !wait_all(B_PFREE + (j & 1), ((j - 2) >> 1) & 1)) break;
       uint8_t* pbuf = smem + OFF_P + (j & 1) * 2 * kNAtom;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -369,7 +376,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   bool have_o = false;
   uint32_t ov[16];
   if (tid < kSoftThreads && live && nt > 0 && !*abort_flag &&
-      mbar_wait(bar(B_O), 0, abort_flag, kWaitLimitNs)) {
+      __all_sync(0xffffffffu, mbar_wait(bar(B_O), 0, abort_flag, kWaitLimitNs))) {
     tc_fence_after();
     tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + TM_O, ov);
     tmem_wait_ld();

@@ -341,7 +341,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // key either in the prefix or inside every row's window.
       const bool full = (k0 + BN - 1 <= qh) &&
                         ((k0 + BN - 1 < m) || (max(k0, m) > qh + BM - 1 - n));
-      if (!mbar_wait(bar(B_S + half), j & 1, abort_flag, kWaitLimitNs)) {
+      // The warp agrees on the outcome, so no lane reaches the warp-wide
+      // TMEM loads alone.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar(B_S + half), j & 1, abort_flag, kWaitLimitNs))) {
         ok = false;
         break;
       }
@@ -427,7 +430,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       mbar_arrive(bar(B_P + half));
     }
     // Epilogue: O / l -> bf16 -> global.
-    if (ok && tr.nt > 0 && mbar_wait(bar(B_O + half), 0, abort_flag, kWaitLimitNs)) {
+    if (ok && tr.nt > 0 &&
+        __all_sync(0xffffffffu,
+                   mbar_wait(bar(B_O + half), 0, abort_flag, kWaitLimitNs))) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       __nv_bfloat16* orow = O + ((row0 + i) * H + h) * HD;
