@@ -312,9 +312,11 @@ def events_time(fn, stream, iters, flush=None):
 GRAPH_STEPS = 16
 
 
-def run_long_prefix_decode(dev, peaks):
-    """B 1, H 10, d 128, n 128: per-step fused decode latency for prefixes of
-    4, 16 and 40 pages (the decode that follows a multi-page prefill)."""
+def run_long_prefix_decode(dev, peaks, layers=12):
+    """B 1, H 10, d 128, n 128: one fused decode step through every layer's
+    cache (12 layers, as a multi-page model decodes after its prefill) for
+    prefixes of 4, 16 and 40 pages.  The 12 caches (up to 0.64 GB) do not
+    stay in L2, so each step reads them from HBM."""
     import torch
     import sliding_window_attention_02_gb300 as rswa
     import workloads
@@ -324,23 +326,34 @@ def run_long_prefix_decode(dev, peaks):
     o = torch.empty(1, H, d, dtype=torch.bfloat16, device=dev)
     rows = []
     for m in (1056, 4128, 10272):
-        _, K, V = workloads.qkv(m + n, H, d, 0, 1.0, torch.bfloat16, device=dev)
-        c = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16, device=dev)
-        c.prefill(None, K, V, None, [m], n, stream=s)
+        caches = []
+        for layer in range(layers):
+            _, K, V = workloads.qkv(m + n, H, d, layer, 1.0, torch.bfloat16,
+                                    device=dev)
+            c = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+            c.prefill(None, K, V, None, [m], n, stream=s)
+            caches.append(c)
+            del K, V
         idx = [0]
 
         def step():
             i = idx[0] % 16
             idx[0] += 1
-            c.decode_step_fused(steps[0][i][None], steps[1][i][None],
-                                steps[2][i][None], o, stream=s)
+            for c in caches:
+                c.decode_step_fused(steps[0][i][None], steps[1][i][None],
+                                    steps[2][i][None], o, stream=s)
         ms = graph_step_ms(step, s, 16, 5)
-        nbytes = H * d * 2 * (2 * (m + n) + 4)
-        rows.append({"m": m, "us_per_step": round(ms * 1e3, 2),
-                     "GB_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1)})
-        del c, K, V
-    return {"workload": "B1 H10 d128 n128 bf16 fused decode, prefix of 4/16/40 "
-                        "pages (latency-bound: 2-53 MB per step)",
+        nbytes = layers * H * d * 2 * (2 * (m + n) + 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"m": m, "us_per_layer": round(ms * 1e3 / layers, 2),
+                     "GB_per_s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
+        del caches
+        torch.cuda.empty_cache()
+    return {"workload": "B1 H10 d128 n128 bf16 fused decode through %d layers' "
+                        "caches, prefix of 4/16/40 pages (%.2f GB per step at "
+                        "40 pages, from HBM)" % (
+                            layers, layers * 10 * 128 * 2 * 2 * (10272 + 128) / 1e9),
             "points": rows}
 
 
