@@ -132,32 +132,6 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
       : "memory");
 }
 
-// 128 columns in four loads and one wait.  The empty asm statements after
-// the wait re-define the registers so no use can move above the wait.
-__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t* r) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t* q = r + 32 * c;
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(q[0]), "=r"(q[1]), "=r"(q[2]), "=r"(q[3]), "=r"(q[4]), "=r"(q[5]),
-          "=r"(q[6]), "=r"(q[7]), "=r"(q[8]), "=r"(q[9]), "=r"(q[10]), "=r"(q[11]),
-          "=r"(q[12]), "=r"(q[13]), "=r"(q[14]), "=r"(q[15]), "=r"(q[16]),
-          "=r"(q[17]), "=r"(q[18]), "=r"(q[19]), "=r"(q[20]), "=r"(q[21]),
-          "=r"(q[22]), "=r"(q[23]), "=r"(q[24]), "=r"(q[25]), "=r"(q[26]),
-          "=r"(q[27]), "=r"(q[28]), "=r"(q[29]), "=r"(q[30]), "=r"(q[31])
-        : "r"(taddr + 32 * c)
-        : "memory");
-  }
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int c = 0; c < 128; c += 8)
-    asm volatile(""
-                 : "+r"(r[c]), "+r"(r[c + 1]), "+r"(r[c + 2]), "+r"(r[c + 3]),
-                   "+r"(r[c + 4]), "+r"(r[c + 5]), "+r"(r[c + 6]), "+r"(r[c + 7]));
-}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(

@@ -43,10 +43,10 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // Thread-block clusters: rank and size of this CTA's cluster, the two halves
-// of the cluster barrier, and the cluster address of `p` in CTA `rank`.  An arrive with release semantics followed
-// by a wait with acquire semantics makes every shared-memory write issued
-// before the arrive (local or remote) visible to every CTA after the wait; a
-// relaxed arrive orders nothing and only marks this CTA as started.
+// of the cluster barrier, and the cluster address of `p` in CTA `rank`.  An
+// arrive with release semantics followed by a wait with acquire semantics
+// makes every shared-memory write issued before the arrive (local or remote,
+// mbarrier initialisation included) visible to every CTA after the wait.
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -56,9 +56,6 @@ __device__ __forceinline__ uint32_t cluster_size() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
-}
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
