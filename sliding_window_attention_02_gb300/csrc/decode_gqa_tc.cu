@@ -314,10 +314,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       float* rm = red_max + (j & 1) * 4 * NQ;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float v = s[g];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+        const float v = warp_max(s[g]);
         if (lane == 0) rm[warp * NQ + g] = v;
       }
       if (!soft_sync()) break;
