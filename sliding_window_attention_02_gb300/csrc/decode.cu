@@ -127,15 +127,8 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   __syncthreads();
   if (s_last) {
     __threadfence();
-    float Mx = -INFINITY;
-    for (int k = 0; k < nch; ++k) Mx = fmaxf(Mx, __ldcg(P + k * (D + 2)));
-    const float r2 = (Mx == -INFINITY) ? 0.f : Mx;
-    float Lt = 0.f, At = 0.f;
-    for (int k = 0; k < nch; ++k) {
-      const float sc = fast_exp2(__ldcg(P + k * (D + 2)) - r2);
-      Lt += __ldcg(P + k * (D + 2) + 1) * sc;
-      if (tid < D) At += __ldcg(P + k * (D + 2) + 2 + tid) * sc;
-    }
+    float r2, Lt, At;
+    merge_partials<1, 8>(P, 0, nch, D, tid, 1, &r2, &Lt, &At);
     if (tid < D) o[bh * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
     if (tid == 0) {
       if (lse) lse[bh] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;

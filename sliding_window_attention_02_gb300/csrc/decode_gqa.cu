@@ -141,20 +141,15 @@ __device__ __forceinline__ void gqa_combine(const CacheView& cv,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  float M[G], L[G], A[G];
+  merge_partials<G, 1>(
+      cv.part + ck.bh0 * cv.max_chunks * (D + 2), (size_t)cv.max_chunks * (D + 2),
+      ck.nch, D, tid, G, M, L, A);
+#pragma unroll
   for (int g = 0; g < G; ++g) {
-    const float* P = cv.part + (ck.bh0 + g) * cv.max_chunks * (D + 2);
-    float Mx = -INFINITY;
-    for (int k = 0; k < ck.nch; ++k) Mx = fmaxf(Mx, __ldcg(P + k * (D + 2)));
-    const float r2 = (Mx == -INFINITY) ? 0.f : Mx;
-    float Lt = 0.f, At = 0.f;
-    for (int k = 0; k < ck.nch; ++k) {
-      const float sc = fast_exp2(__ldcg(P + k * (D + 2)) - r2);
-      Lt += __ldcg(P + k * (D + 2) + 1) * sc;
-      if (tid < D) At += __ldcg(P + k * (D + 2) + 2 + tid) * sc;
-    }
-    if (tid < D) o[(ck.bh0 + g) * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
+    if (tid < D) o[(ck.bh0 + g) * D + tid] = (T)(L[g] > 0.f ? A[g] / L[g] : 0.f);
     if (tid == 0) {
-      if (lse) lse[ck.bh0 + g] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;
+      if (lse) lse[ck.bh0 + g] = L[g] > 0.f ? (M[g] + log2f(L[g])) * kLn2 : -INFINITY;
       // Every CTA of this head group read t_b before its own arrival.
       if (FUSED) cv.t_dev[ck.bh0 + g] = ck.t_b + 1;
     }

@@ -86,7 +86,7 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
 }
 
 template <bool FUSED, int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, CacheView cv,
                      const __nv_bfloat16* __restrict__ q,
@@ -409,20 +409,16 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   __syncthreads();
   if (*s_last && tid < kSoftThreads) {
     __threadfence();
-    for (int g = 0; g < per_kv && g < G; ++g) {
-      const float* P = cv.part + (bh0 + g) * cv.max_chunks * (HD + 2);
-      float Mx = -INFINITY;
-      for (int k = 0; k < nch; ++k) Mx = fmaxf(Mx, __ldcg(P + k * (HD + 2)));
-      const float r2 = (Mx == -INFINITY) ? 0.f : Mx;
-      float Lt = 0.f, At = 0.f;
-      for (int k = 0; k < nch; ++k) {
-        const float sc = fast_exp2(__ldcg(P + k * (HD + 2)) - r2);
-        Lt += __ldcg(P + k * (HD + 2) + 1) * sc;
-        At += __ldcg(P + k * (HD + 2) + 2 + tid) * sc;
-      }
-      o[(bh0 + g) * HD + tid] = __float2bfloat16(Lt > 0.f ? At / Lt : 0.f);
+    float M[G], L[G], A[G];
+    merge_partials<G, (G <= 2 ? 2 : 1)>(
+        cv.part + bh0 * cv.max_chunks * (HD + 2), (size_t)cv.max_chunks * (HD + 2),
+        nch, HD, tid, per_kv, M, L, A);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (g >= per_kv) break;
+      o[(bh0 + g) * HD + tid] = __float2bfloat16(L[g] > 0.f ? A[g] / L[g] : 0.f);
       if (tid == 0) {
-        if (lse) lse[bh0 + g] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;
+        if (lse) lse[bh0 + g] = L[g] > 0.f ? (M[g] + log2f(L[g])) * kLn2 : -INFINITY;
         // Every CTA of this KV head read t_b before its own arrival.
         if (FUSED) cv.t_dev[bh0 + g] = t_b + 1;
       }

@@ -194,4 +194,58 @@ struct SoftmaxState {
   }
 };
 
+// Online merge of split-K partials (m, l, acc[D]) in log2 units: chunks
+// 0..nch-1 of NG heads, head g's chunk k at P0 + g * hs + k * (D + 2); this
+// thread's column is col (acc ignored when col >= D).  KB chunks of every
+// head are loaded before any of them is used, so a merge costs
+// ceil(nch / KB) load round trips rather than two per chunk.  On return
+// M[g] is the reference maximum, L[g] the sum and A[g] the column, both
+// relative to M[g] (L[g] = 0 for a head with no visible key).
+template <int NG, int KB>
+__device__ __forceinline__ void merge_partials(const float* P0, size_t hs,
+                                               int nch, int D, int col,
+                                               int ng, float* M, float* L,
+                                               float* A) {
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    M[g] = -INFINITY;
+    L[g] = 0.f;
+    A[g] = 0.f;
+  }
+  for (int k0 = 0; k0 < nch; k0 += KB) {
+    float mk[NG][KB], lk[NG][KB], ak[NG][KB];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        mk[g][u] = -INFINITY;
+        lk[g][u] = 0.f;
+        ak[g][u] = 0.f;
+        if (g < ng && k0 + u < nch) {
+          const float* P = P0 + g * hs + (size_t)(k0 + u) * (D + 2);
+          mk[g][u] = __ldcg(P);
+          lk[g][u] = __ldcg(P + 1);
+          if (col < D) ak[g][u] = __ldcg(P + 2 + col);
+        }
+      }
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float mn = M[g];
+#pragma unroll
+      for (int u = 0; u < KB; ++u) mn = fmaxf(mn, mk[g][u]);
+      const float ref = (mn == -INFINITY) ? 0.f : mn;
+      const float sc = fast_exp2(M[g] - ref);
+      L[g] *= sc;
+      A[g] *= sc;
+#pragma unroll
+      for (int u = 0; u < KB; ++u) {
+        const float w = fast_exp2(mk[g][u] - ref);
+        L[g] += lk[g][u] * w;
+        A[g] += ak[g][u] * w;
+      }
+      M[g] = mn;
+    }
+  }
+}
+
 }  // namespace rswa
