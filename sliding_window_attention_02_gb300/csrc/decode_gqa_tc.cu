@@ -124,6 +124,16 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   __syncthreads();                                  // barriers initialised
   griddep_wait();
 
+  // The query rows of the KV head's heads (column tid), loaded alongside the
+  // state words: their address does not depend on them.
+  __nv_bfloat16 qv[G];
+  if (tid < kSoftThreads) {
+    const size_t bq = (size_t)b * cv.H + (size_t)kv * per_kv;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      qv[g] = g < per_kv ? q[(bq + g) * HD + tid] : __float2bfloat16(0.f);
+  }
+
   // This chunk: slab rows [j0, j1) of KV head (b, kv).
   const int64_t m_b = cv.m_dev[b];
   const int chunk = cv.chunk;
@@ -187,8 +197,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     // Q_G^T as the MMA's B operand: row g = query head g, K-major over d.
 #pragma unroll
     for (int g = 0; g < NQ; ++g) {
-      const __nv_bfloat16 v =
-          (live && g < per_kv) ? q[(bh0 + g) * HD + tid] : __float2bfloat16(0.f);
+      const __nv_bfloat16 v = (live && g < G) ? qv[g < G ? g : 0] : __float2bfloat16(0.f);
       *reinterpret_cast<__nv_bfloat16*>(smem + OFF_Q + sw128_off(g, tid, kNAtom)) = v;
     }
     fence_proxy_async_smem();
