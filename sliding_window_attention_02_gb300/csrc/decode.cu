@@ -128,7 +128,9 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   if (s_last) {
     __threadfence();
     float r2, Lt, At;
-    merge_partials<1, 8>(P, 0, nch, D, tid, 1, &r2, &Lt, &At);
+    // Up to 16 chunks per round trip: a batch-1 head with a 40-page prefix
+    // has 42 chunks, and this merge is the last step of the decode.
+    merge_partials<1, 16>(P, 0, nch, D, tid, 1, &r2, &Lt, &At);
     if (tid < D) o[bh * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
     if (tid == 0) {
       if (lse) lse[bh] = Lt > 0.f ? (r2 + log2f(Lt)) * kLn2 : -INFINITY;
