@@ -10,7 +10,7 @@
 // with both accumulators in TMEM, K and V tiles streaming through a TMA ring,
 // and the CUDA cores left with the softmax: one key per thread, G scores.
 //
-// Grid (max_chunks, H_kv, B): one CTA is one split-K chunk (prefix chunk or
+// Grid (B * H_kv, max_chunks): one CTA is one split-K chunk (prefix chunk or
 // ring chunk, as in decode_kernel) of one KV head and serves every query
 // head of that KV head, so the CTA that stores a fused step's new key and
 // value in its ring slot is also the only reader of that slot: it writes the
@@ -107,7 +107,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tid = threadIdx.x;
-  const int c = blockIdx.x, kv = blockIdx.y, b = blockIdx.z;
+  const int b = blockIdx.x / cv.Hkv, kv = blockIdx.x % cv.Hkv;
   const int per_kv = cv.H / cv.Hkv;                 // query heads served (<= G)
 
   if (tid == 0) {
@@ -139,7 +139,15 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   const int chunk = cv.chunk;
   const int cp = (int)((m_b + chunk - 1) / chunk);
   const int nch = cp + (int)((cv.n + chunk - 1) / chunk);
-  const bool live = c < nch;
+  // Grid slot y: prefix chunk y while y < ceil(m_cap / chunk) (no work past
+  // this sequence's prefix), then ring chunk y - ceil(m_cap / chunk).  Slots
+  // launch in order, so every sequence's prefix chunks run before the
+  // one-tile ring chunks, which fill the last wave.  c is the chunk's index
+  // among this sequence's nch partials.
+  const int cp_cap = (int)((cv.m_cap + chunk - 1) / chunk);
+  const int y = blockIdx.y;
+  const bool live = y >= cp_cap || y < cp;
+  const int c = y < cp_cap ? y : cp + (y - cp_cap);
   const size_t bh0 = (size_t)b * cv.H + (size_t)kv * per_kv;
   const size_t bkv = (size_t)b * cv.Hkv + kv;
   const int64_t t_b = cv.t_dev[bh0];                // equal for the heads
@@ -458,7 +466,7 @@ cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cv.max_chunks, cv.Hkv, cv.B);
+  cfg.gridDim = dim3(cv.B * cv.Hkv, cv.max_chunks);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
