@@ -95,7 +95,7 @@ int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
 // 128..256 keys each (measured best on GB300 for one sequence with a 1K-10K
 // key cache; shorter caches take the cluster path).
 #ifndef RSWA_TC_WAVES
-#define RSWA_TC_WAVES 4
+#define RSWA_TC_WAVES 2
 #endif
 
 int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
