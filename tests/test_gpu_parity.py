@@ -552,6 +552,34 @@ def test_gqa_decode_tc_multitile(cuda_lib):
         assert cache.get_t(b) == T
 
 
+@pytest.mark.parametrize("dtype", [1, 0], ids=["bf16-tc", "f32"])
+def test_gqa_decode_empty_ring(cuda_lib, dtype):
+    """decode_step right after a prefix-only prefill (t_b = 0, nothing
+    appended): every ring chunk is empty, so the grouped kernels publish
+    empty partials for it and the output is attention over the prefix."""
+    rswa = cuda_lib
+    B, H, Hkv, d, n = 24, 8, 2, 128, 16
+    m_list = [200 + 31 * b for b in range(B)]
+    rows = sum(m_list)
+    Q, K, V = _qkv_gqa(rows + B, H, Hkv, d, seed=66, dtype=tdt(dtype))
+    offs = np.cumsum([0] + m_list)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, dtype, kv_heads=Hkv)
+    cache.prefill(None, K[:rows].cuda(), V[:rows].cuda(), None, m_list, 0)
+    q = Q[rows:rows + B].contiguous().cuda()
+    o = torch.empty(B, H, d, dtype=tdt(dtype), device="cuda")
+    lse = torch.empty(B, H, device="cuda")
+    cache.decode_step(q, o, lse)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b in [0, 7, 23]:
+        st = oracle.prefill_cache(f64(K[offs[b]:offs[b + 1]]), f64(V[offs[b]:offs[b + 1]]),
+                                  m_list[b], n, 0)
+        ro, rl = oracle.decode_step(st, f64(q[b]), n)
+        assert_close(f64(o[b]), ro, dtype, f"seq {b}")
+        assert np.abs(f64(lse[b]) - rl).max() <= (1e-4 if dtype == 0 else 1e-3)
+        assert cache.get_t(b) == 0
+
+
 def test_gqa_decode_block(cuda_lib):
     rswa = cuda_lib
     B, H, Hkv, d, n = 2, 8, 4, 128, 32

@@ -18,25 +18,32 @@ pytestmark = pytest.mark.gpu
 BF16_MAX, BF16_MEAN = 2e-2, 5e-3
 
 
-def _two_caches(rswa, m_list, n, H, d, seed):
+def _two_caches(rswa, m_list, n, H, d, seed, Hkv=None):
     B = len(m_list)
     rows = sum(m_list)
-    _, K, V = workloads.qkv(rows, H, d, seed, 1.0, torch.bfloat16, device="cuda")
+    Hkv = H if Hkv is None else Hkv
+    K = workloads.normal((rows, Hkv, d), 3 * seed + 1, 1.0, torch.bfloat16, "cuda")
+    V = workloads.normal((rows, Hkv, d), 3 * seed + 2, 1.0, torch.bfloat16, "cuda")
     caches = []
     for _ in range(2):
-        c = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16)
+        c = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
         c.prefill(None, K, V, None, m_list, 0)
         caches.append(c)
     return caches
 
 
-@pytest.mark.parametrize("m_list,n", [([288], 128), ([300, 17, 1029], 16)])
-def test_static_scratch_matches_fused(cuda_lib, m_list, n):
+@pytest.mark.parametrize("m_list,n,Hkv", [([288], 128, 4), ([300, 17, 1029], 16, 4),
+                                          ([300, 17, 1029], 16, 1)])
+def test_static_scratch_matches_fused(cuda_lib, m_list, n, Hkv):
+    # Hkv = 1: four query heads over one KV head (the grouped decode path).
     rswa = cuda_lib
     H, d = 4, 128
     B = len(m_list)
-    ref_cache, static_cache = _two_caches(rswa, m_list, n, H, d, seed=3)
-    steps = workloads.qkv(2 * B, H, d, 44, 1.0, torch.bfloat16, device="cuda")
+    ref_cache, static_cache = _two_caches(rswa, m_list, n, H, d, seed=3, Hkv=Hkv)
+    q_all = workloads.normal((2 * B, H, d), 132, 1.0, torch.bfloat16, "cuda")
+    k_all = workloads.normal((2 * B, Hkv, d), 133, 1.0, torch.bfloat16, "cuda")
+    v_all = workloads.normal((2 * B, Hkv, d), 134, 1.0, torch.bfloat16, "cuda")
+    steps = (q_all, k_all, v_all)
     for call in range(2):
         q, k, v = (x[call * B:(call + 1) * B].contiguous() for x in steps)
         o_ref = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
