@@ -571,9 +571,19 @@ def oracle_single_page_sample(budget_s, max_steps=None):
             "decode_s_per_step": t_dec}
 
 
-def run_cpu_worker(budget_s, max_steps=None):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
-               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+def host_cores():
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_worker(budget_s, max_steps=None, threads=1):
+    """The oracle in a subprocess with `threads` BLAS/OpenMP threads."""
+    t = str(int(threads))
+    env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t,
+               MKL_NUM_THREADS=t, CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker",
            str(budget_s)]
     if max_steps:
@@ -663,10 +673,12 @@ def main_ours(args):
     rswa.load()
     peaks, peak_src = load_peaks()
 
-    # CPU baseline first (subprocess, one thread) on rank 0
-    cpu = None
+    # CPU baseline first (subprocess; one thread, then every core) on rank 0
+    cpu = cpu_all = None
+    ncores = host_cores()
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = run_cpu_worker(args.cpu_budget)
+        cpu_all = run_cpu_worker(args.cpu_budget, threads=ncores)
 
     sp = setup_single_page(dev)
     w = sp["w"]
@@ -755,6 +767,13 @@ def main_ours(args):
                            "(%.1f ms/step) of the same workload, float64, one "
                            "thread, extrapolated to 6000 steps"
                            % (cpu["decode_steps"], 1e3 * cpu["decode_s_per_step"]))},
+            "cpu_baseline_all_cores": None if cpu_all is None else {
+                "value": round(cpu_all["tokens_per_s"], 2), "unit": "tokens/s",
+                "cores": ncores, "kind": "oracle",
+                "sample": ("as cpu_baseline, with %d BLAS/OpenMP threads "
+                           "(%d decode steps, %.1f ms/step)"
+                           % (ncores, cpu_all["decode_steps"],
+                              1e3 * cpu_all["decode_s_per_step"]))},
             "e2e": e2e,
             "gpu_launches": args.steps * (2 + w.T),
             "clocks": clocks,
