@@ -579,6 +579,73 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def oracle_config_samples(rows_prefill=128):
+    """Oracle (one thread) on the other workloads, each a bounded sample:
+    one fused decode step of the batched and of the sweep workload (every
+    sequence; cache contents are constant arrays of the right shapes, as the
+    time does not depend on the values), and `rows_prefill` seeded rows of
+    one multi-page prefill layer, extrapolated to 12 layers by the number of
+    visible (query, key) pairs."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    rng = np.random.default_rng(0)
+    out = {}
+
+    def decode_all(B, H, d, m_list, n, T):
+        states = []
+        for m in m_list:
+            states.append({"Kp": np.full((m, H, d), 0.01),
+                           "Vp": np.full((m, H, d), 0.02),
+                           "Kr": np.full((n, H, d), 0.01),
+                           "Vr": np.full((n, H, d), 0.02), "t": T})
+        q = np.full((B, H, d), 0.03)
+        t0 = time.perf_counter()
+        for b, st in enumerate(states):
+            oracle.decode_step_fused(st, q[b], q[b, :], q[b, :], n)
+        return time.perf_counter() - t0
+
+    w = workloads.WORKLOADS["batched_decode_bf16"]
+    m_list = workloads.prefix_lengths(w.batch, *w.m_range, seed=0)
+    out["batched_decode"] = {"s_per_step": round(
+        decode_all(w.batch, w.heads, w.head_dim, m_list, w.n, w.T), 4)}
+    w = workloads.WORKLOADS["decode_sweep_bf16"]
+    out["decode_sweep"] = {"s_per_step": round(
+        decode_all(w.batch, w.heads, w.head_dim, [w.m] * w.batch, w.n, 4096), 4)}
+    w = workloads.WORKLOADS["multipage_prefill_bf16"]
+    L = w.m + w.T
+    Q, K, V = workloads.qkv(L, w.heads, w.head_dim, 0, 1.0, torch.bfloat16)
+    Q, K, V = (x.double().numpy() for x in (Q, K, V))
+    rows = sorted(rng.choice(L, size=rows_prefill, replace=False).tolist())
+    t0 = time.perf_counter()
+    oracle.prefill_attention(Q, K, V, w.m, w.n, rows=rows)
+    el = time.perf_counter() - t0
+    def pairs(i):   # |N(i)|: i + 1 in the prefix, m + min(n, i - m + 1) after
+        return i + 1 if i < w.m else w.m + min(w.n, i - w.m + 1)
+    sample_pairs = sum(pairs(i) for i in rows)
+    total_pairs = sum(pairs(i) for i in range(L))
+    out["prefill"] = {"sample_rows": rows_prefill, "sample_s": round(el, 3),
+                      "s_per_layer": round(el * total_pairs / sample_pairs, 1),
+                      "s_12_layers": round(12 * el * total_pairs / sample_pairs, 1)}
+    return out
+
+
+def run_cpu_configs_worker():
+    """oracle_config_samples in a one-thread subprocess without the GPU."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__),
+                        "--cpu-configs-worker"], capture_output=True, text=True,
+                       env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = 1
+    out["kind"] = "oracle"
+    return out
+
+
 def run_cpu_worker(budget_s, max_steps=None, threads=1):
     """The oracle in a subprocess with `threads` BLAS/OpenMP threads."""
     t = str(int(threads))
@@ -679,6 +746,9 @@ def main_ours(args):
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = run_cpu_worker(args.cpu_budget)
         cpu_all = run_cpu_worker(args.cpu_budget, threads=ncores)
+    cpu_configs = None
+    if rank == 0 and ws == 1 and not args.no_cpu and not args.no_extras:
+        cpu_configs = run_cpu_configs_worker()
 
     sp = setup_single_page(dev)
     w = sp["w"]
@@ -745,6 +815,8 @@ def main_ours(args):
         del sp
         torch.cuda.empty_cache()
         extras = run_extras(dev, peaks, quick=args.quick)
+        if cpu_configs is not None:
+            extras["cpu_oracle"] = cpu_configs
 
     if rank == 0:
         line = {
@@ -897,6 +969,7 @@ def main():
     ap.add_argument("--quick", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--cpu-worker", type=float, default=None)
+    ap.add_argument("--cpu-configs-worker", action="store_true")
     ap.add_argument("--cpu-max-steps", type=int, default=None)
     ap.add_argument("--only", default=None,
                     choices=["single_page", "batched", "sweep", "gqa", "prefill"],
@@ -905,6 +978,9 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="prefill layers with --only prefill")
     args = ap.parse_args()
+    if args.cpu_configs_worker:
+        print(json.dumps(oracle_config_samples()))
+        return 0
     if args.cpu_worker is not None:
         print(json.dumps(oracle_single_page_sample(args.cpu_worker,
                                                    args.cpu_max_steps)))
