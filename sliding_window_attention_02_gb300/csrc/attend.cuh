@@ -39,6 +39,88 @@ __device__ __forceinline__ void load_q_frag(const T* q_row, int lane,
   for (int e = 0; e < C::EPL; ++e) qf[e] *= sc;
 }
 
+// One batch of a warp's rows for attend_range: this lane's 16-byte slices
+// of the U rows of K and V its lane group takes, and which of them are keys.
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
+struct AttendBatch {
+  uint4 k[UNROLL], v[UNROLL];
+  bool ok[UNROLL];
+};
+
+// Load the batch starting at logical row `base` (see attend_range for the
+// row mapping); rows at or past j_end are flagged and read row j_begin.
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
+__device__ __forceinline__ void attend_load(
+    const T* __restrict__ Kb, const T* __restrict__ Vb, int64_t stride,
+    int64_t base, int64_t j_begin, int64_t j_end, int64_t sub_row,
+    const T* knew, const T* vnew, int lane, int64_t seg_end, int64_t gap,
+    AttendBatch<T, D, UNROLL>& bt) {
+  using C = AttendCfg<T, D, UNROLL>;
+  constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
+  const int grp = lane / LPK;
+  const int col = (lane % LPK) * EPL;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int64_t row = base + u * KPW + grp;
+    bt.ok[u] = row < j_end;
+    const int64_t lr = bt.ok[u] ? row : j_begin;
+    const int64_t r = lr < seg_end ? lr : lr + gap;
+    const T* kp = Kb + r * stride + col;
+    const T* vp = Vb + r * stride + col;
+    if (r == sub_row) {
+      kp = knew + col;
+      vp = vnew + col;
+    }
+    bt.k[u] = ld_stream16(kp);
+    bt.v[u] = ld_stream16(vp);
+  }
+}
+
+// Fold a loaded batch into this lane's online-softmax state.
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
+__device__ __forceinline__ void attend_consume(
+    const float* qf, const AttendBatch<T, D, UNROLL>& bt,
+    SoftmaxState<AttendCfg<T, D>::EPL>& st) {
+  using C = AttendCfg<T, D, UNROLL>;
+  constexpr int EPL = C::EPL, LPK = C::LPK, U = C::U;
+  float s[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    float kf[EPL];
+    Elt<T>::widen(bt.k[u], kf);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
+    s[u] = acc;
+  }
+#pragma unroll
+  for (int off = LPK / 2; off > 0; off >>= 1) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
+  }
+  float mx = st.m;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (!bt.ok[u]) s[u] = -INFINITY;
+    mx = fmaxf(mx, s[u]);
+  }
+  const float ref = (mx == -INFINITY) ? 0.f : mx;
+  const float alpha = fast_exp2(st.m - ref);
+  st.l *= alpha;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) st.acc[e] *= alpha;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const float p = fast_exp2(s[u] - ref);
+    st.l += p;
+    float vf[EPL];
+    Elt<T>::widen(bt.v[u], vf);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) st.acc[e] = fmaf(p, vf[e], st.acc[e]);
+  }
+  st.m = mx;
+}
+
 // Attend logical rows [j_begin, j_end) of a key/value table whose physical
 // row p starts at Kb + p * stride (elements); logical row r maps to
 // p = r for r < seg_end and p = r + gap beyond it (two segments of one
@@ -52,64 +134,11 @@ __device__ __forceinline__ void attend_range(
     int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
     SoftmaxState<AttendCfg<T, D>::EPL>& st, int64_t seg_end = INT64_MAX,
     int64_t gap = 0) {
-  using C = AttendCfg<T, D, UNROLL>;
-  constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
-  const int grp = lane / LPK;
-  const int col = (lane % LPK) * EPL;
   for (int64_t base = j_begin + first; base < j_end; base += step) {
-    uint4 kr[U], vr[U];
-    bool ok[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t row = base + u * KPW + grp;
-      ok[u] = row < j_end;
-      const int64_t lr = ok[u] ? row : j_begin;
-      const int64_t r = lr < seg_end ? lr : lr + gap;
-      const T* kp = Kb + r * stride + col;
-      const T* vp = Vb + r * stride + col;
-      if (r == sub_row) {
-        kp = knew + col;
-        vp = vnew + col;
-      }
-      kr[u] = ld_stream16(kp);
-      vr[u] = ld_stream16(vp);
-    }
-    float s[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float kf[EPL];
-      Elt<T>::widen(kr[u], kf);
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc = fmaf(qf[e], kf[e], acc);
-      s[u] = acc;
-    }
-#pragma unroll
-    for (int off = LPK / 2; off > 0; off >>= 1) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], off);
-    }
-    float mx = st.m;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (!ok[u]) s[u] = -INFINITY;
-      mx = fmaxf(mx, s[u]);
-    }
-    const float ref = (mx == -INFINITY) ? 0.f : mx;
-    const float alpha = fast_exp2(st.m - ref);
-    st.l *= alpha;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) st.acc[e] *= alpha;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const float p = fast_exp2(s[u] - ref);
-      st.l += p;
-      float vf[EPL];
-      Elt<T>::widen(vr[u], vf);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) st.acc[e] = fmaf(p, vf[e], st.acc[e]);
-    }
-    st.m = mx;
+    AttendBatch<T, D, UNROLL> bt;
+    attend_load<T, D, UNROLL>(Kb, Vb, stride, base, j_begin, j_end, sub_row, knew,
+                              vnew, lane, seg_end, gap, bt);
+    attend_consume<T, D, UNROLL>(qf, bt, st);
   }
 }
 

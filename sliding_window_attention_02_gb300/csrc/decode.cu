@@ -18,7 +18,11 @@ namespace rswa {
 // At least 5 resident CTAs per SM: measured best on GB300 for the batched
 // and long-output workloads (it also steers the compiler to issue a warp's
 // loads ahead of their use).
-template <typename T, int D, bool FUSED>
+// PREFETCH: the preceding kernel of the stream writes no prefix row and no
+// m_b of this cache (the host's per-handle flag), so a prefix-chunk CTA
+// reads m_b and loads its warps' first row batch before the dependency
+// wait, while the previous kernel drains.
+template <typename T, int D, bool FUSED, bool PREFETCH>
 __global__ void __launch_bounds__(kDecodeThreads, 5)
 decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
               const T* __restrict__ vnew, T* __restrict__ o,
@@ -27,11 +31,29 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   constexpr int NW = kDecodeThreads / 32;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = cv.H / cv.Hkv;                  // query heads per KV head
+  const size_t bkv = (size_t)b * cv.Hkv + h / grp;
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
+  AttendBatch<T, D> pre;
+  bool have_pre = false;
+  int64_t m_b = 0;
+  if (PREFETCH) {
+    m_b = cv.m_dev[b];
+    const int64_t j0 = (int64_t)c * cv.chunk;
+    const int64_t j1 = min(j0 + cv.chunk, m_b);
+    const int64_t base = j0 + (int64_t)warp * C::KEYS_WARP;
+    if (j0 < m_b && base < j1) {                  // a prefix chunk with rows here
+      attend_load<T, D>(Kb, Vb, D, base, j0, j1, -1, nullptr, nullptr, lane,
+                        INT64_MAX, 0, pre);
+      have_pre = true;
+    }
+  }
   // Launched as a programmatic dependent: wait until the previous kernel in
   // the stream has completed and its writes are visible.
   griddep_wait();
 
-  const int64_t m_b = cv.m_dev[b];
+  if (!PREFETCH) m_b = cv.m_dev[b];
   const int chunk = cv.chunk;
   const int cp = (int)((m_b + chunk - 1) / chunk);
   const int cr = (int)((cv.n + chunk - 1) / chunk);
@@ -39,11 +61,6 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   if (c >= nch) return;
   const size_t bh = (size_t)b * cv.H + h;
   const int64_t t_b = cv.t_dev[bh];
-  const int grp = cv.H / cv.Hkv;                  // query heads per KV head
-  const size_t bkv = (size_t)b * cv.Hkv + h / grp;
-
-  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
   const T* kn = FUSED ? knew + bkv * D : nullptr;
   const T* vn = FUSED ? vnew + bkv * D : nullptr;
 
@@ -82,8 +99,13 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   load_q_frag<T, D>(q + bh * D, lane, qf);
   SoftmaxState<C::EPL> st;
   st.init();
-  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, (int64_t)warp * C::KEYS_WARP,
-                     (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane, st);
+  int64_t first = (int64_t)warp * C::KEYS_WARP;
+  if (have_pre) {
+    attend_consume<T, D>(qf, pre, st);
+    first += (int64_t)NW * C::KEYS_WARP;
+  }
+  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, first, (int64_t)NW * C::KEYS_WARP, sub,
+                     kn, vn, lane, st);
   // The next step's kernel may start launching; it waits for this one.
   griddep_launch_dependents();
   merge_groups<T, D>(st);
@@ -479,13 +501,23 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
       e = launch_cluster<T, D, false>(cv, qq, nullptr, nullptr, oo, lse,
                                       prefetch, s);
   } else {
-    dim3 grid(cv.max_chunks, cv.H, cv.B);
-    if (fused)
-      e = launch_pdl(decode_kernel<T, D, true>, grid, dim3(kDecodeThreads), 0, s,
-                     cv, qq, kk, vv, oo, lse);
+    const dim3 grid(cv.max_chunks, cv.H, cv.B), block(kDecodeThreads);
+    const T* nk = nullptr;
+    // The preloaded batch costs registers: bf16 caches only (float32 ones
+    // would spill).
+    prefetch = prefetch && sizeof(T) == 2;
+    if (fused && prefetch)
+      e = launch_pdl(decode_kernel<T, D, true, true>, grid, block, 0, s, cv, qq, kk,
+                     vv, oo, lse);
+    else if (fused)
+      e = launch_pdl(decode_kernel<T, D, true, false>, grid, block, 0, s, cv, qq, kk,
+                     vv, oo, lse);
+    else if (prefetch)
+      e = launch_pdl(decode_kernel<T, D, false, true>, grid, block, 0, s, cv, qq, nk,
+                     nk, oo, lse);
     else
-      e = launch_pdl(decode_kernel<T, D, false>, grid, dim3(kDecodeThreads), 0, s,
-                     cv, qq, (const T*)nullptr, (const T*)nullptr, oo, lse);
+      e = launch_pdl(decode_kernel<T, D, false, false>, grid, block, 0, s, cv, qq, nk,
+                     nk, oo, lse);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
