@@ -28,13 +28,21 @@ def f64(t):
     return t.detach().double().cpu().numpy()
 
 
+def _worst(got, ref, err):
+    """Where the largest error sits, with both values there."""
+    idx = np.unravel_index(int(np.nanargmax(np.where(np.isfinite(err), err, np.inf))),
+                           err.shape)
+    return f"at {tuple(int(i) for i in idx)}: got {float(got[idx]):.6g}, oracle {float(ref[idx]):.6g}"
+
+
 def assert_close(got, ref, dtype, what=""):
-    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
-    assert np.isfinite(err).all(), f"{what}: non-finite output"
+    got = np.asarray(got, dtype=np.float64)
+    err = np.abs(got - ref)
+    assert np.isfinite(err).all(), f"{what}: non-finite output {_worst(got, ref, err)}"
     if dtype == 0:
-        assert err.max() <= F32_TOL, f"{what}: max {err.max():.3e}"
+        assert err.max() <= F32_TOL, f"{what}: max {err.max():.3e} {_worst(got, ref, err)}"
     else:
-        assert err.max() <= BF16_MAX, f"{what}: max {err.max():.3e}"
+        assert err.max() <= BF16_MAX, f"{what}: max {err.max():.3e} {_worst(got, ref, err)}"
         assert err.mean() <= BF16_MEAN, f"{what}: mean {err.mean():.3e}"
 
 
