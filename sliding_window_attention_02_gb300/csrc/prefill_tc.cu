@@ -33,12 +33,6 @@
 #include "rswa_device.cuh"
 #include "tc_ptx.cuh"
 
-// 1: the softmax's row maximum with three-input max and its exp2 argument
-// and row sum with packed f32x2 arithmetic; 0: scalar.
-#ifndef RSWA_PREFILL_PACKED
-#define RSWA_PREFILL_PACKED 1
-#endif
-
 namespace rswa {
 namespace {
 
@@ -347,7 +341,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           }
           tmem_st32(s_addr + c0, v);
         }
-#if RSWA_PREFILL_PACKED
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           mx[0] = fmax3(mx[0], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
@@ -355,15 +348,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           mx[2] = fmax3(mx[2], __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
           mx[3] = fmax3(mx[3], __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
         }
-#else
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          mx[0] = fmaxf(mx[0], __uint_as_float(v[e]));
-          mx[1] = fmaxf(mx[1], __uint_as_float(v[e + 1]));
-          mx[2] = fmaxf(mx[2], __uint_as_float(v[e + 2]));
-          mx[3] = fmaxf(mx[3], __uint_as_float(v[e + 3]));
-        }
-#endif
       }
       if (!full) tmem_wait_st();
       const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
@@ -397,7 +381,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       // columns of S_h (two bf16 per column), 64 logits at a time.  Columns
       // 0..63 of S_h are read before any P column is written.
       uint32_t pk[2][32];
-#if RSWA_PREFILL_PACKED
       // Two logits per packed f32x2 FMA and sum.
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(nref, nref);
       uint64_t ps2[2] = {0, 0};
@@ -422,24 +405,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       f2_unpack(ps2[0], s0, s1);
       f2_unpack(ps2[1], s2, s3);
       const float psum = (s0 + s1) + (s2 + s3);
-#else
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t v[64];
-        tmem_ld32_sync(s_addr + 64 * hc, v);
-        tmem_ld32_sync(s_addr + 64 * hc + 32, v + 32);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int e = 2 * c;
-          const float p0 = ex2(fmaf(__uint_as_float(v[e]), sl2, nref));
-          const float p1 = ex2(fmaf(__uint_as_float(v[e + 1]), sl2, nref));
-          ps[c & 3] += p0 + p1;
-          pk[hc][c] = pack_bf16(p0, p1);
-        }
-      }
-      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-#endif
       tmem_st32(s_addr, pk[0]);
       tmem_st32(s_addr + 32, pk[1]);
       l_run += psum;
