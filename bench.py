@@ -357,6 +357,97 @@ def run_long_prefix_decode(dev, peaks, layers=12):
             "points": rows}
 
 
+def run_block_decode(dev, peaks, blocks=(1, 4, 16, 64), reps=16):
+    """Multi-query decode (rswa_decode_block) on the single-page cache: one
+    call decodes and appends `block` consecutive tokens per sequence (the
+    shape of verifying drafted tokens).  Per call latency and tokens/s."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    B, H, d, m, n = w.batch, w.heads, w.head_dim, w.m, w.n
+    s = torch.cuda.Stream(device=dev)
+    rows = []
+    for k in blocks:
+        Q, K, V = workloads.qkv(m + reps * k, H, d, 0, w.std, torch.bfloat16,
+                                device=dev)
+        c = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+        c.prefill(None, K[:m], V[:m], None, [m], 0, stream=s)
+        o = torch.empty(B, k, H, d, dtype=torch.bfloat16, device=dev)
+        blk = [tuple(x[m + i * k:m + (i + 1) * k][None].contiguous()
+                     for x in (Q, K, V)) for i in range(reps)]
+        idx = [0]
+
+        def step():
+            q, kk, vv = blk[idx[0] % reps]
+            idx[0] += 1
+            c.decode_block(q, kk, vv, o, stream=s)
+        ms = graph_step_ms(step, s, reps, 5)
+        rows.append({"block": k, "us_per_call": round(ms * 1e3, 2),
+                     "tokens_per_s": round(B * k / (ms * 1e-3), 1)})
+        del c, Q, K, V
+    return {"workload": "B1 H10 d128 m288 n128 bf16 (single-page cache), "
+                        "rswa_decode_block with blocks of 1/4/16/64 tokens",
+            "points": rows}
+
+
+def run_vanilla_swa(dev, peaks, layers=3):
+    """Vanilla SWA (m = 0: the window slides over every token): a 32K-row
+    prefill (band tiles only) and a batched fused decode step with a full
+    ring, through the same kernels."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    H, d, n, L = 10, 128, 128, 32768
+    s = torch.cuda.Stream(device=dev)
+    pairs = sum(min(n, i + 1) for i in range(L))
+    qkv = [workloads.qkv(L, H, d, 100 + l, 1.0, torch.bfloat16, device=dev)
+           for l in range(layers)]
+    caches = [rswa.RswaCache(0, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+              for _ in range(layers)]
+    outs = [torch.empty(L, H, d, dtype=torch.bfloat16, device=dev)
+            for _ in range(layers)]
+
+    def pstep():
+        for (Q, K, V), c, O in zip(qkv, caches, outs):
+            c.prefill(Q, K, V, O, [0], L, stream=s)
+    with torch.cuda.stream(s):
+        pstep()
+    ms = statistics.mean(events_time(pstep, s, 3)) / layers
+    tf = 4 * d * pairs * H / (ms * 1e-3) / 1e12
+    pre = {"rows": L, "ms_per_layer": round(ms, 4), "visible_pairs_per_head": pairs,
+           "TFLOP_per_s": round(tf, 1),
+           "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    del qkv, caches, outs
+    torch.cuda.empty_cache()
+    # 256 sequences: 170 MB of window per step, more than L2 holds.  The
+    # ring is filled by a prefill of n outputs, then t_b is set to 4096.
+    B, T = 256, 4096
+    _, K, V = workloads.qkv(B * n, H, d, 7, 1.0, torch.bfloat16, device=dev)
+    c = rswa.RswaCache(0, n, H, d, B, rswa.RSWA_BF16, device=dev)
+    c.prefill(None, K, V, None, [0] * B, n, stream=s)
+    torch.cuda.synchronize()
+    c.set_t([T] * B)
+    steps = workloads.qkv(16 * B, H, d, 8, 1.0, torch.bfloat16, device=dev)
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    idx = [0]
+
+    def dstep():
+        i = idx[0] % 16
+        idx[0] += 1
+        c.decode_step_fused(steps[0][i * B:(i + 1) * B], steps[1][i * B:(i + 1) * B],
+                            steps[2][i * B:(i + 1) * B], o, stream=s)
+    ms = graph_step_ms(dstep, s, 16, 5)
+    nbytes = B * H * d * 2 * (2 * n + 4)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    dec = {"batch": B, "us_per_step": round(ms * 1e3, 2), "GB_per_s": round(gbs, 1),
+           "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    return {"workload": "vanilla SWA, m = 0, n = 128, H10 d128 bf16: prefill of "
+                        "32768 rows (%d layers) and a B256 fused decode step "
+                        "with a full ring (t_b 4096)" % layers,
+            "prefill": pre, "decode": dec}
+
+
 def run_mha_baseline(dev, quick=False):
     """R-SWA (n = 128) against the standard full cache (n = T = 6000, i.e.
     every output stays visible: plain causal attention) on the single-page
@@ -510,6 +601,10 @@ def run_extras(dev, peaks, quick=False):
     del sw
     # one sequence decoding over a long prefix (after a multi-page prefill) --
     out["long_prefix_decode"] = run_long_prefix_decode(dev, peaks)
+    torch.cuda.empty_cache()
+    out["block_decode"] = run_block_decode(dev, peaks)
+    torch.cuda.empty_cache()
+    out["vanilla_swa"] = run_vanilla_swa(dev, peaks)
     torch.cuda.empty_cache()
     # standard-MHA baseline (the pages' comparison) -------------------------
     out["mha_baseline"] = run_mha_baseline(dev, quick)

@@ -377,6 +377,10 @@ int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
   if (injected_failure()) return RSWA_ECUDA;
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
+  if (block == 1)  // [B][1][H][d] is the fused single step's [B][H][d]
+    return status_of(launch_decode(cache->cv, q, k, v, o, lse, true,
+                                   cache->prefix_stable.exchange(true),
+                                   static_cast<cudaStream_t>(stream)));
   return status_of(launch_decode_block(cache->cv, q, k, v, block, o, lse,
                                        static_cast<cudaStream_t>(stream)));
 }

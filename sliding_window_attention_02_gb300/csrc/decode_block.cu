@@ -4,24 +4,30 @@
 // window already in the cache, j in [max(0, t_b + i - n + 1), t_b), and to
 // block tokens 0..i (k <= n keeps every earlier block token inside the
 // window).  The attention kernel reads the ring before the append kernel
-// overwrites any slot; both run on the caller's stream in that order.
+// overwrites any slot; both run on the caller's stream in that order, the
+// append kernel waiting on the attention kernel's completion.
 // This is the shape of a speculative-verification forward or of chunked
 // prefill of output text into an existing cache.
 #include "attend.cuh"
 
 namespace rswa {
 
-// One warp per (b, i, h); 4 warps per CTA over consecutive (i, h).
-template <typename T, int D>
-__global__ void __launch_bounds__(128)
+// One CTA of NW warps per (b, i, h): the warps split every key segment of
+// query i (prefix, cached outputs of its window, block tokens 0..i) between
+// them, NW * KEYS_WARP rows per round, and merge in shared memory.
+constexpr int kBlockWarps = 8;
+
+template <typename T, int D, int NW>
+__global__ void __launch_bounds__(NW * 32)
 decode_block_kernel(CacheView cv, const T* __restrict__ q,
                     const T* __restrict__ kblk, const T* __restrict__ vblk,
                     int64_t k, T* __restrict__ o, float* __restrict__ lse) {
   using C = AttendCfg<T, D>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
-  const int64_t qi = (int64_t)blockIdx.x * 4 + warp;
-  if (qi >= k * cv.H) return;
+  const int64_t qi = blockIdx.x;                         // i * H + h
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t i = qi / cv.H;
   const int h = (int)(qi % cv.H);
   const size_t bh = (size_t)b * cv.H + h;
@@ -32,6 +38,8 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
   const int64_t n = cv.n;
   const int64_t row_stride = (int64_t)cv.Hkv * D;        // k, v: [B][k][Hkv][D]
   const size_t qrow = ((size_t)b * k + i) * cv.H + h;    // q, o: [B][k][H][D]
+  const int64_t first = (int64_t)warp * C::KEYS_WARP;
+  const int64_t step = (int64_t)NW * C::KEYS_WARP;
 
   float qf[C::EPL];
   load_q_frag<T, D>(q + qrow * D, lane, qf);
@@ -40,8 +48,8 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
   const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
   const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
   // prefix
-  attend_range<T, D>(qf, Kb, Vb, D, 0, m_b, 0, C::KEYS_WARP, -1, nullptr,
-                     nullptr, lane, st);
+  attend_range<T, D>(qf, Kb, Vb, D, 0, m_b, first, step, -1, nullptr, nullptr,
+                     lane, st);
   // cached outputs of the window: j in [j_lo, t_b), slot j mod n
   const int64_t j_lo = max((int64_t)0, t_b + i - n + 1);
   if (j_lo < t_b) {
@@ -49,55 +57,102 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
     const T* Vr = Vb + cv.m_cap * D;
     const int64_t a = j_lo % n, cnt = t_b - j_lo;
     const int64_t first_end = min(n, a + cnt);
-    attend_range<T, D>(qf, Kr, Vr, D, a, first_end, 0, C::KEYS_WARP, -1, nullptr,
+    attend_range<T, D>(qf, Kr, Vr, D, a, first_end, first, step, -1, nullptr,
                        nullptr, lane, st);
     if (a + cnt > n)
-      attend_range<T, D>(qf, Kr, Vr, D, 0, a + cnt - n, 0, C::KEYS_WARP, -1,
-                         nullptr, nullptr, lane, st);
+      attend_range<T, D>(qf, Kr, Vr, D, 0, a + cnt - n, first, step, -1, nullptr,
+                         nullptr, lane, st);
   }
-  // block tokens 0..i (rows of the input, stride H*D)
+  // block tokens 0..i (rows of the input, stride H_kv * D)
   const T* Kk = kblk + ((size_t)b * k * cv.Hkv + kvh) * D;
   const T* Vk = vblk + ((size_t)b * k * cv.Hkv + kvh) * D;
-  attend_range<T, D>(qf, Kk, Vk, row_stride, 0, i + 1, 0, C::KEYS_WARP, -1,
-                     nullptr, nullptr, lane, st);
+  attend_range<T, D>(qf, Kk, Vk, row_stride, 0, i + 1, first, step, -1, nullptr,
+                     nullptr, lane, st);
   merge_groups<T, D>(st);
+  __shared__ float s_m[NW], s_l[NW];
+  __shared__ float s_acc[NW][D];
   if (lane < C::LPK) {
-    float out[C::EPL];
-    const float inv = 1.f / st.l;
 #pragma unroll
-    for (int e = 0; e < C::EPL; ++e) out[e] = st.acc[e] * inv;
-    *reinterpret_cast<uint4*>(o + qrow * D + lane * C::EPL) = Elt<T>::narrow(out);
-    if (lane == 0 && lse) lse[qrow] = (st.m + log2f(st.l)) * kLn2;
+    for (int e = 0; e < C::EPL; ++e) s_acc[warp][lane * C::EPL + e] = st.acc[e];
+    if (lane == 0) {
+      s_m[warp] = st.m;
+      s_l[warp] = st.l;
+    }
+  }
+  __syncthreads();
+  const int tid = threadIdx.x;
+  if (tid < D) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, s_m[w]);
+    const float ref = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, A = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float sc = fast_exp2(s_m[w] - ref);
+      L += s_l[w] * sc;
+      A += s_acc[w][tid] * sc;
+    }
+    o[qrow * D + tid] = (T)(A / L);          // self is always visible: L > 0
+    if (tid == 0 && lse) lse[qrow] = (ref + log2f(L)) * kLn2;
   }
 }
 
-// One CTA per sequence: block token i -> ring slot (t_b + i) mod n for every
-// KV head, then t_b += k for every query head (after every thread has read
-// t_b).
+// One CTA per (block token i, sequence b): token i -> ring slot
+// (t_b + i) mod n for every KV head.  Each CTA reads t_b before it counts
+// itself done on the sequence's counter; the last of the k CTAs sets
+// t_b += k for every query head and rearms the counter.  The writes wait for
+// the attention kernel (programmatic dependent launch), which reads slots
+// that later block tokens overwrite.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 append_block_kernel(CacheView cv, const T* __restrict__ kblk,
-                    const T* __restrict__ vblk, int64_t k) {
-  const int b = blockIdx.x;
-  const int H = cv.Hkv;                          // k, v carry the KV heads
+                    const T* __restrict__ vblk, int k) {
+  griddep_wait();
+  const int i = blockIdx.x, b = blockIdx.y;
+  const int Hkv = cv.Hkv;                        // k, v carry the KV heads
   const int64_t t_b = cv.t_dev[(size_t)b * cv.H];
-  constexpr int NV = D * sizeof(T) / 16;
-  const int64_t total = 2 * k * H * NV;
-  for (int64_t x = threadIdx.x; x < total; x += blockDim.x) {
-    const int kv = (int)(x / (k * H * NV));
-    const int64_t rest = x % (k * H * NV);
-    const int64_t i = rest / (H * NV);
-    const int h = (int)((rest / NV) % H);
-    const int vi = (int)(rest % NV);
-    const T* in = (kv ? vblk : kblk) + (((size_t)b * k + i) * H + h) * D;
-    const int64_t slot = (t_b + i) % cv.n;
+  constexpr int NV = D * (int)sizeof(T) / 16;
+  const int per_kv = Hkv * NV;
+  const size_t slot = (size_t)((t_b + i) % cv.n);
+  const size_t in_row = ((size_t)b * k + i) * Hkv;
+  for (int x = threadIdx.x; x < 2 * per_kv; x += blockDim.x) {
+    const int kv = x >= per_kv;
+    const int r = x - kv * per_kv;
+    const int h = r / NV, vi = r % NV;
+    const T* in = (kv ? vblk : kblk) + (in_row + h) * D;
     T* out = static_cast<T*>(kv ? cv.V : cv.K) +
-             (((size_t)b * H + h) * cv.slab_rows + cv.m_cap + slot) * D;
+             (((size_t)b * Hkv + h) * cv.slab_rows + cv.m_cap + slot) * D;
     reinterpret_cast<uint4*>(out)[vi] = reinterpret_cast<const uint4*>(in)[vi];
   }
   __syncthreads();
-  for (int h = threadIdx.x; h < cv.H; h += blockDim.x)
-    cv.t_dev[(size_t)b * cv.H + h] = t_b + k;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int32_t* cnt = cv.cnt_bh + (size_t)b * cv.H;
+    if (atomicAdd(cnt, 1) == k - 1) {
+      __threadfence();
+      for (int h = 0; h < cv.H; ++h) cv.t_dev[(size_t)b * cv.H + h] = t_b + k;
+      *cnt = 0;
+    }
+  }
+}
+
+// Programmatic stream serialization: a kernel may begin launching while the
+// previous kernel of the stream drains; each one waits (griddepcontrol) before
+// it touches memory that the previous one writes.
+template <typename K, typename... Args>
+static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t s,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <typename T, int D>
@@ -105,13 +160,14 @@ static cudaError_t launch_block_t(const CacheView& cv, const void* q,
                                   const void* k, const void* v, int64_t block,
                                   void* o, float* lse, cudaStream_t s) {
   const int64_t nq = block * cv.H;
-  dim3 grid((unsigned)((nq + 3) / 4), (unsigned)cv.B);
-  decode_block_kernel<T, D><<<grid, 128, 0, s>>>(cv, (const T*)q, (const T*)k,
-                                                 (const T*)v, block, (T*)o, lse);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(decode_block_kernel<T, D, kBlockWarps>,
+                             dim3((unsigned)nq, (unsigned)cv.B),
+                             dim3(kBlockWarps * 32), s, cv, (const T*)q,
+                             (const T*)k, (const T*)v, block, (T*)o, lse);
   if (e != cudaSuccess) return e;
-  append_block_kernel<T, D><<<cv.B, 128, 0, s>>>(cv, (const T*)k, (const T*)v, block);
-  return cudaGetLastError();
+  return launch_pdl(append_block_kernel<T, D>,
+                    dim3((unsigned)block, (unsigned)cv.B), dim3(128), s, cv,
+                    (const T*)k, (const T*)v, (int)block);
 }
 
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
