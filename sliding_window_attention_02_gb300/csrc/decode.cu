@@ -134,6 +134,15 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     Ls += s_l[w] * sc;
     if (tid < D) A += s_acc[w][tid] * sc;
   }
+  if (nch == 1) {
+    // The only chunk of (b, h) (a short cache, e.g. m_b = 0): no partials.
+    if (tid < D) o[bh * D + tid] = (T)(Ls > 0.f ? A / Ls : 0.f);
+    if (tid == 0) {
+      if (lse) lse[bh] = Ls > 0.f ? (ref + log2f(Ls)) * kLn2 : -INFINITY;
+      if (FUSED) cv.t_dev[bh] = t_b + 1;
+    }
+    return;
+  }
 
   // Publish this chunk's partial (m, l, acc[D]).
   float* P = cv.part + (bh * cv.max_chunks) * (D + 2);

@@ -7,12 +7,17 @@
 // ("Unlimited-OCR deep dive": N(t) = P U D_n(t); "Unlimited OCR", GeekNews:
 // the two-segment window of size m + n).
 //
-// One CTA owns two adjacent 128-row query tiles ("halves") of one head and
+// A work unit is two adjacent 128-row query tiles ("halves") of one head; it
 // walks the union of their key tiles: the prefix tiles 0 .. ceil(m/128)-1 up
 // to the diagonal, then the band tiles that hold the last n keys of the
 // output rows.  Tiles the mask excludes entirely are never loaded.  Both
 // halves share every K and V tile.  Per-element masking runs only on tiles
-// the mask covers partially for that half.
+// the mask covers partially for that half.  A CTA takes one unit per round
+// of gridDim.x units of the heavy-first order (a snake order, see
+// snake_unit), and its producer loads the next unit's Q and first K/V tiles
+// while the current unit's last tiles and epilogue run.  The host launches
+// one CTA per SM when units are short (few key tiles: band-dominated
+// sequences), else one CTA per unit.
 //
 // Roles (320 threads):
 //   warps 0-3   softmax of half 0 (thread r owns row r = TMEM lane r)
@@ -26,9 +31,15 @@
 // keeps the tensor core on one half while the other half's softmax runs, and
 // relies on the in-order execution of one thread's tcgen05.mma stream for
 // S_h being rewritten only after PV_h has read P_h.
+// Across units: Q is reloaded once the last QK MMA of the unit has completed
+// (B_QFREE), and PV_h of a unit's first tile overwrites O_h only after the
+// softmax warps of half h have read the previous unit's O_h (B_OFREE).
 // Every wait is bounded; on a timeout the CTA drains its own copies and MMAs,
 // frees TMEM, sets the cache's device error flag and exits.
 #include <cuda.h>
+
+#include <algorithm>
+#include <climits>
 
 #include "rswa_device.cuh"
 #include "tc_ptx.cuh"
@@ -57,6 +68,8 @@ __host__ __device__ constexpr uint32_t tm_o(int half) { return half ? 384u : 256
 constexpr uint32_t TM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// Below this mean number of key tiles per unit the launch is persistent.
+constexpr int64_t kPersistentTilesPerUnit = 16;
 
 // barrier indices
 constexpr int B_Q = 0;
@@ -66,7 +79,9 @@ constexpr int B_S = B_EMPTY + NS;              // 2 halves
 constexpr int B_P = B_S + 2;                   // 2 halves
 constexpr int B_O = B_P + 2;                   // 2 halves
 constexpr int B_FIN = B_O + 2;
-constexpr int NBAR = B_FIN + 1;
+constexpr int B_QFREE = B_FIN + 1;             // Q buffer may be reloaded
+constexpr int B_OFREE = B_QFREE + 1;           // 2 halves: O_h read out
+constexpr int NBAR = B_OFREE + 2;
 
 struct TileRange {
   int np;        // prefix tiles 0 .. np-1
@@ -95,6 +110,42 @@ __device__ __forceinline__ TileRange tile_range(int r_lo, int r_hi, int m, int n
 
 __device__ __forceinline__ int tile_at(const TileRange& t, int j) {
   return j < t.np ? j : t.kb_start + (j - t.np);
+}
+
+// The k-th unit of CTA b out of G: rounds of G units, walked forward in even
+// rounds and backward in odd ones, so that with units in heavy-first order
+// every CTA's sum of work is near the mean (as list scheduling would give,
+// with no shared counter).  -1 past the last unit.
+__device__ __forceinline__ int snake_unit(int k, int b, int G, int units) {
+  const int u = k * G + ((k & 1) ? G - 1 - b : b);
+  return u < units ? u : -1;
+}
+
+// Work unit u: head u % H, tile pair total_pairs - 1 - u / H (heavy pairs
+// first: a pair's work grows with its position in the sequence).
+struct Unit {
+  int h, kvh, m, L, q0;
+  int64_t row0;
+  TileRange tr;
+};
+
+__device__ __forceinline__ Unit unit_at(int u, const CacheView& cv,
+                                        const SeqTable& st, int total_pairs) {
+  Unit w;
+  const int H = cv.H;
+  w.h = u % H;
+  const int g = total_pairs - 1 - u / H;
+  int sl = 0;
+  while (sl + 1 < st.nseq && st.tile_off[sl + 1] <= g) ++sl;
+  const int pr = g - st.tile_off[sl];                      // pair in sequence
+  w.m = st.m[sl];
+  const int n = (int)min(cv.n, (int64_t)1 << 30);
+  w.L = w.m + (int)st.T[sl];
+  w.kvh = w.h / (H / cv.Hkv);                              // KV head read
+  w.row0 = st.row_off[sl];
+  w.q0 = pr * 2 * BM;
+  w.tr = tile_range(w.q0, w.q0 + 2 * BM - 1, w.m, n, w.L);
+  return w;
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 (bf16, f32 accumulate).
@@ -146,6 +197,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// PERSIST: a CTA may take several units (one per round of gridDim units);
+// otherwise exactly one, unit blockIdx.x, and the cross-unit barriers
+// (B_QFREE, B_OFREE) and phase counters fold away.
+template <bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
@@ -164,22 +219,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = cv.H;
-  const int h = blockIdx.x % H;
-  const int g = total_pairs - 1 - (int)(blockIdx.x / H);  // heavy pairs first
-  int sl = 0;
-  while (sl + 1 < st.nseq && st.tile_off[sl + 1] <= g) ++sl;
-  const int pr = g - st.tile_off[sl];                      // pair in sequence
-  const int m = st.m[sl];
-  const int n = (int)min(cv.n, (int64_t)1 << 30);
-  const int L = m + (int)st.T[sl];
-  const int kvh = h / (H / cv.Hkv);                         // KV head read
-  const int64_t row0 = st.row_off[sl];
-  const int q0 = pr * 2 * BM;
-  const TileRange tr = tile_range(q0, q0 + 2 * BM - 1, m, n, L);
+  const int units = total_pairs * H;
+  constexpr int kMaxRounds = PERSIST ? INT_MAX : 1;
 
   if (threadIdx.x == 0) {
-    for (int k = 0; k < NBAR; ++k)
-      mbar_init(bar(k), (k == B_P || k == B_P + 1) ? 128u : 1u);
+    for (int k = 0; k < NBAR; ++k) {
+      const bool per_row = k == B_P || k == B_P + 1 || k == B_OFREE || k == B_OFREE + 1;
+      mbar_init(bar(k), per_row ? 128u : 1u);
+    }
     *abort_flag = 0;
     *never = 0;
     fence_mbar_init();
@@ -200,31 +247,44 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      const int x0 = h * HD;                                 // Q column
-      const int xk = kvh * HD;                               // K, V column
-      const int yq = (int)(row0 + q0);
-      mbar_arrive_expect_tx(bar(B_Q), 2 * kTileB);
-      tma_load_2d(sb + OFF_Q, &tmQ, x0, yq, bar(B_Q));
-      tma_load_2d(sb + OFF_Q + kSub, &tmQ, x0 + 64, yq, bar(B_Q));
-      tma_load_2d(sb + OFF_Q + kTileB, &tmQ, x0, yq + BM, bar(B_Q));
-      tma_load_2d(sb + OFF_Q + kTileB + kSub, &tmQ, x0 + 64, yq + BM, bar(B_Q));
-      int issued = 0;
-      for (int idx = 0; idx < 2 * tr.nt; ++idx) {
-        const int s = idx % NS;
-        if (idx >= NS && !mbar_wait(bar(B_EMPTY + s), ((idx / NS) - 1) & 1,
-                                    abort_flag, kWaitLimitNs))
+      uint32_t gi = 0, nq = 0;                  // K/V loads, Q loads issued
+      bool ok = true;
+      for (int k = 0, u; ok && k < kMaxRounds && (u = snake_unit(k, blockIdx.x, gridDim.x, units)) >= 0;
+           ++k) {
+        const Unit w = unit_at(u, cv, st, total_pairs);
+        if (w.tr.nt == 0) continue;
+        // Q of the previous unit is read by its last QK MMA.
+        if (nq > 0 && !mbar_wait(bar(B_QFREE), (nq - 1) & 1, abort_flag, kWaitLimitNs))
           break;
-        const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
-        const int y = (int)(row0 + (int64_t)tile_at(tr, idx >> 1) * BN);
-        const uint32_t dst = sb + OFF_RING + s * kTileB;
-        mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
-        tma_load_2d(dst, map, xk, y, bar(B_FULL + s));
-        tma_load_2d(dst + kSub, map, xk + 64, y, bar(B_FULL + s));
-        ++issued;
+        const int x0 = w.h * HD;                               // Q column
+        const int xk = w.kvh * HD;                             // K, V column
+        const int yq = (int)(w.row0 + w.q0);
+        mbar_arrive_expect_tx(bar(B_Q), 2 * kTileB);
+        tma_load_2d(sb + OFF_Q, &tmQ, x0, yq, bar(B_Q));
+        tma_load_2d(sb + OFF_Q + kSub, &tmQ, x0 + 64, yq, bar(B_Q));
+        tma_load_2d(sb + OFF_Q + kTileB, &tmQ, x0, yq + BM, bar(B_Q));
+        tma_load_2d(sb + OFF_Q + kTileB + kSub, &tmQ, x0 + 64, yq + BM, bar(B_Q));
+        ++nq;
+        for (int idx = 0; idx < 2 * w.tr.nt; ++idx, ++gi) {
+          const uint32_t s = gi % NS;
+          if (gi >= (uint32_t)NS &&
+              !mbar_wait(bar(B_EMPTY + s), ((gi / NS) - 1) & 1, abort_flag,
+                         kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
+          const int y = (int)(w.row0 + (int64_t)tile_at(w.tr, idx >> 1) * BN);
+          const uint32_t dst = sb + OFF_RING + s * kTileB;
+          mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
+          tma_load_2d(dst, map, xk, y, bar(B_FULL + s));
+          tma_load_2d(dst + kSub, map, xk + 64, y, bar(B_FULL + s));
+        }
       }
-      // Drain: every copy issued has landed before the CTA may exit.
-      mbar_wait(bar(B_Q), 0, never, kWaitLimitNs);
-      for (int idx = max(0, issued - NS); idx < issued; ++idx)
+      // Drain: every copy issued has landed before the CTA may exit (older
+      // loads of a ring slot completed before the slot was reissued).
+      if (nq > 0) mbar_wait(bar(B_Q), (nq - 1) & 1, never, kWaitLimitNs);
+      for (uint32_t idx = gi > (uint32_t)NS ? gi - NS : 0; idx < gi; ++idx)
         mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, never, kWaitLimitNs);
     }
   } else if (warp == kMmaWarp) {
@@ -232,13 +292,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, HD, true);
-      auto wait_slot = [&](int idx) {
-        return mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, abort_flag,
-                         kWaitLimitNs);
+      auto wait = [&](int k, uint32_t phase) {
+        return mbar_wait(bar(k), phase & 1, abort_flag, kWaitLimitNs);
       };
-      // S_h = Q_h K^T from the K tile in ring slot of load idx.
-      auto qk = [&](int half, int idx) {
-        const uint32_t kb = sb + OFF_RING + (idx % NS) * kTileB;
+      auto wait_slot = [&](uint32_t gi) { return wait(B_FULL + gi % NS, gi / NS); };
+      // S_h = Q_h K^T from the K tile in the ring slot of load gi.
+      auto qk = [&](int half, uint32_t gi) {
+        const uint32_t kb = sb + OFF_RING + (gi % NS) * kTileB;
         const uint32_t qb = sb + OFF_Q + half * kTileB;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
@@ -248,50 +308,69 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         mma_commit(bar(B_S + half));
       };
-      // O_h (+)= P_h V from TMEM P_h and the V tile of load idx.
-      auto pv = [&](int half, int idx, bool acc) {
-        const uint32_t vb = sb + OFF_RING + (idx % NS) * kTileB;
+      // O_h (+)= P_h V from TMEM P_h and the V tile of load gi.
+      auto pv = [&](int half, uint32_t gi, bool acc) {
+        const uint32_t vb = sb + OFF_RING + (gi % NS) * kTileB;
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_bf16_ts(tmem + tm_o(half), tmem + tm_s(half) + k * 8,
                       desc_sw128(vb + k * 2048, kSub, 1024), idesc_pv,
                       (acc || k > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(bar(B_Q), 0, abort_flag, kWaitLimitNs) && tr.nt > 0;
-      if (ok) {
+      uint32_t gi = 0, gt = 0, kq = 0;          // loads, tiles, units done
+      bool ok = true;
+      for (int k = 0, u; ok && k < kMaxRounds && (u = snake_unit(k, blockIdx.x, gridDim.x, units)) >= 0;
+           ++k) {
+        const Unit w = unit_at(u, cv, st, total_pairs);
+        const int nt = w.tr.nt;
+        if (nt == 0) continue;
+        if (!wait(B_Q, kq) || !wait_slot(gi)) break;
         tc_fence_after();
-        ok = wait_slot(0);
-        if (ok) {
+        qk(0, gi);
+        qk(1, gi);
+        mma_commit(bar(B_EMPTY + gi % NS));
+        if (nt == 1) mma_commit(bar(B_QFREE));
+        for (int j = 0; j < nt; ++j) {
+          const uint32_t vi = gi + 2 * j + 1, ki = gi + 2 * j + 2;
+          const bool more = j + 1 < nt;
+          // PV_h of the unit's first tile overwrites O_h: the previous
+          // unit's epilogue must have read it.
+          if (!wait(B_P + 0, gt + j) || !wait_slot(vi) ||
+              (j == 0 && kq > 0 && !wait(B_OFREE + 0, kq - 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          qk(0, 0);
-          qk(1, 0);
-          mma_commit(bar(B_EMPTY + 0));
-        }
-      }
-      for (int j = 0; ok && j < tr.nt; ++j) {
-        const int vi = 2 * j + 1, ki = 2 * j + 2;
-        const bool more = j + 1 < tr.nt;
-        if (!mbar_wait(bar(B_P + 0), j & 1, abort_flag, kWaitLimitNs) || !wait_slot(vi))
-          break;
-        tc_fence_after();
-        pv(0, vi, j > 0);
-        if (more) {
-          if (!wait_slot(ki)) break;
+          pv(0, vi, j > 0);
+          if (more) {
+            if (!wait_slot(ki)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            qk(0, ki);
+          } else {
+            mma_commit(bar(B_O + 0));
+          }
+          if (!wait(B_P + 1, gt + j) ||
+              (j == 0 && kq > 0 && !wait(B_OFREE + 1, kq - 1))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          qk(0, ki);
-        } else {
-          mma_commit(bar(B_O + 0));
+          pv(1, vi, j > 0);
+          mma_commit(bar(B_EMPTY + vi % NS));
+          if (more) {
+            qk(1, ki);
+            mma_commit(bar(B_EMPTY + ki % NS));
+            if (j + 2 == nt) mma_commit(bar(B_QFREE));   // last QK of the unit
+          } else {
+            mma_commit(bar(B_O + 1));
+          }
         }
-        if (!mbar_wait(bar(B_P + 1), j & 1, abort_flag, kWaitLimitNs)) break;
-        tc_fence_after();
-        pv(1, vi, j > 0);
-        mma_commit(bar(B_EMPTY + vi % NS));
-        if (more) {
-          qk(1, ki);
-          mma_commit(bar(B_EMPTY + ki % NS));
-        } else {
-          mma_commit(bar(B_O + 1));
-        }
+        gi += 2 * nt;
+        gt += nt;
+        ++kq;
       }
       // Drain: all MMAs of this CTA have finished before TMEM is freed.
       mma_commit(bar(B_FIN));
@@ -302,139 +381,152 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int half = warp >> 2;
     const int r = threadIdx.x & 127;                    // row in half
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int qh = q0 + half * BM;                      // first row of half
-    const int i = qh + r;                               // row in sequence
     const float sl2 = rsqrtf((float)HD) * kLog2e;
     const uint32_t s_addr = tmem + lane_off + tm_s(half);
     const uint32_t o_addr = tmem + lane_off + tm_o(half);
-    float m_run = -INFINITY, l_run = 0.f;
+    uint32_t gt = 0, kq = 0;                            // tiles, units done
     bool ok = true;
-    for (int j = 0; j < tr.nt; ++j) {
-      const int k0 = tile_at(tr, j) * BN;
-      // Tile fully visible for this half: every key <= every row, and every
-      // key either in the prefix or inside every row's window.
-      const bool full = (k0 + BN - 1 <= qh) &&
-                        ((k0 + BN - 1 < m) || (max(k0, m) > qh + BM - 1 - n));
-      // The warp agrees on the outcome, so no lane reaches the warp-wide
-      // TMEM loads alone.
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(bar(B_S + half), j & 1, abort_flag, kWaitLimitNs))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // Pass 1: row maximum over the visible logits, 32 columns at a time.
-      const int hi = i - k0;   // visible: c <= hi && (c < a || c > b)
-      const int a = m - k0;
-      const int b = i - n - k0;
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    for (int k = 0, u; ok && k < kMaxRounds && (u = snake_unit(k, blockIdx.x, gridDim.x, units)) >= 0;
+           ++k) {
+      const Unit w = unit_at(u, cv, st, total_pairs);
+      const TileRange& tr = w.tr;
+      if (tr.nt == 0) continue;
+      const int m = w.m;
+      const int n = (int)min(cv.n, (int64_t)1 << 30);
+      const int qh = w.q0 + half * BM;                  // first row of half
+      const int i = qh + r;                             // row in sequence
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < tr.nt; ++j) {
+        const int k0 = tile_at(tr, j) * BN;
+        // Tile fully visible for this half: every key <= every row, and every
+        // key either in the prefix or inside every row's window.
+        const bool full = (k0 + BN - 1 <= qh) &&
+                          ((k0 + BN - 1 < m) || (max(k0, m) > qh + BM - 1 - n));
+        // The warp agrees on the outcome, so no lane reaches the warp-wide
+        // TMEM loads alone.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + half), (gt + j) & 1,
+                                               abort_flag, kWaitLimitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // Pass 1: row maximum over the visible logits, 32 columns at a time.
+        const int hi = i - k0;   // visible: c <= hi && (c < a || c > b)
+        const int a = m - k0;
+        const int b = i - n - k0;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32_sync(s_addr + c0, v);
-        if (!full) {
-          // Mask in place and write back, so pass 2 reads masked logits.
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32_sync(s_addr + c0, v);
+          if (!full) {
+            // Mask in place and write back, so pass 2 reads masked logits.
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int c = c0 + e;
-            if (!(c <= hi && (c < a || c > b))) v[e] = 0xff800000u;  // -inf
+            for (int e = 0; e < 32; ++e) {
+              const int c = c0 + e;
+              if (!(c <= hi && (c < a || c > b))) v[e] = 0xff800000u;  // -inf
+            }
+            tmem_st32(s_addr + c0, v);
           }
-          tmem_st32(s_addr + c0, v);
-        }
 #pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          mx[0] = fmax3(mx[0], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
-          mx[1] = fmax3(mx[1], __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-          mx[2] = fmax3(mx[2], __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
-          mx[3] = fmax3(mx[3], __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+          for (int e = 0; e < 32; e += 8) {
+            mx[0] = fmax3(mx[0], __uint_as_float(v[e]), __uint_as_float(v[e + 1]));
+            mx[1] = fmax3(mx[1], __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            mx[2] = fmax3(mx[2], __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
+            mx[3] = fmax3(mx[3], __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
+          }
         }
-      }
-      if (!full) tmem_wait_st();
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
-      // Lazy rescale: keep the reference maximum unless it grew by > 2^8.
-      // Exact either way: O and l share the reference.  O_h is stable here:
-      // S_h(j) completing implies PV_h(j-1) completed (one MMA stream).
-      float alpha = 1.f;
-      bool resc = false;
-      const float m_new = fmaxf(m_run, tmax);
-      if (m_run == -INFINITY) {
-        m_run = m_new;
-      } else if (m_new > m_run + kRescaleThreshold) {
-        alpha = ex2(m_run - m_new);
-        m_run = m_new;
-        l_run *= alpha;
-        resc = true;
-      }
-      const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (!full) tmem_wait_st();
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        // Lazy rescale: keep the reference maximum unless it grew by > 2^8.
+        // Exact either way: O and l share the reference.  O_h is stable here:
+        // S_h(j) completing implies PV_h(j-1) completed (one MMA stream).
+        float alpha = 1.f;
+        bool resc = false;
+        const float m_new = fmaxf(m_run, tmax);
+        if (m_run == -INFINITY) {
+          m_run = m_new;
+        } else if (m_new > m_run + kRescaleThreshold) {
+          alpha = ex2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+          resc = true;
+        }
+        const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32_sync(o_addr + c * 32, o);
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32_sync(o_addr + c * 32, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(o_addr + c * 32, o);
+            for (int e = 0; e < 32; ++e)
+              o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(o_addr + c * 32, o);
+          }
         }
-      }
-      // Pass 2: P_h = exp2(x - ref) as bf16 -> TMEM over the first 64
-      // columns of S_h (two bf16 per column), 64 logits at a time.  Columns
-      // 0..63 of S_h are read before any P column is written.
-      uint32_t pk[2][32];
-      // Two logits per packed f32x2 FMA and sum.
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(nref, nref);
-      uint64_t ps2[2] = {0, 0};
+        // Pass 2: P_h = exp2(x - ref) as bf16 -> TMEM over the first 64
+        // columns of S_h (two bf16 per column), 64 logits at a time.  Columns
+        // 0..63 of S_h are read before any P column is written.
+        uint32_t pk[2][32];
+        // Two logits per packed f32x2 FMA and sum.
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(nref, nref);
+        uint64_t ps2[2] = {0, 0};
 #pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        uint32_t v[64];
-        tmem_ld32_sync(s_addr + 64 * hc, v);
-        tmem_ld32_sync(s_addr + 64 * hc + 32, v + 32);
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t v[64];
+          tmem_ld32_sync(s_addr + 64 * hc, v);
+          tmem_ld32_sync(s_addr + 64 * hc + 32, v + 32);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int e = 2 * c;
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
-                           sl2x2, nref2),
-                    x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ps2[c & 1] = f2_add(ps2[c & 1], f2_pack(p0, p1));
-          pk[hc][c] = pack_bf16(p0, p1);
+          for (int c = 0; c < 32; ++c) {
+            const int e = 2 * c;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                             sl2x2, nref2),
+                      x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            ps2[c & 1] = f2_add(ps2[c & 1], f2_pack(p0, p1));
+            pk[hc][c] = pack_bf16(p0, p1);
+          }
         }
+        float s0, s1, s2, s3;
+        f2_unpack(ps2[0], s0, s1);
+        f2_unpack(ps2[1], s2, s3);
+        const float psum = (s0 + s1) + (s2 + s3);
+        tmem_st32(s_addr, pk[0]);
+        tmem_st32(s_addr + 32, pk[1]);
+        l_run += psum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(B_P + half));
       }
-      float s0, s1, s2, s3;
-      f2_unpack(ps2[0], s0, s1);
-      f2_unpack(ps2[1], s2, s3);
-      const float psum = (s0 + s1) + (s2 + s3);
-      tmem_st32(s_addr, pk[0]);
-      tmem_st32(s_addr + 32, pk[1]);
-      l_run += psum;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_P + half));
-    }
-    // Epilogue: O / l -> bf16 -> global.
-    if (ok && tr.nt > 0 &&
-        __all_sync(0xffffffffu,
-                   mbar_wait(bar(B_O + half), 0, abort_flag, kWaitLimitNs))) {
+      if (!ok) break;
+      // Epilogue: O / l -> bf16 -> global, then O_h is free for the next unit.
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar(B_O + half), kq & 1, abort_flag, kWaitLimitNs)))
+        break;
       tc_fence_after();
       const float inv = 1.f / l_run;
-      __nv_bfloat16* orow = O + ((row0 + i) * H + h) * HD;
+      __nv_bfloat16* orow = O + ((w.row0 + i) * H + w.h) * HD;
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t o[32];
         tmem_ld32_sync(o_addr + c * 32, o);
-        if (i < L) {
-          uint32_t w[16];
+        if (i < w.L) {
+          uint32_t wv[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv,
-                             __uint_as_float(o[2 * e + 1]) * inv);
+            wv[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv,
+                              __uint_as_float(o[2 * e + 1]) * inv);
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            dst[e] = make_uint4(wv[4 * e], wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
         }
       }
+      tc_fence_before();
+      mbar_arrive(bar(B_OFREE + half));
+      gt += tr.nt;
+      ++kq;
     }
   }
 
@@ -491,6 +583,29 @@ bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Key tiles visited by all tile pairs of the launch (one head): the host
+// twin of tile_range, summed over the pairs.
+static int64_t host_tiles(const SeqTable& st, int64_t n_window) {
+  const int64_t n = std::min<int64_t>(n_window, int64_t(1) << 30);
+  int64_t total = 0;
+  for (int sq = 0; sq < st.nseq; ++sq) {
+    const int64_t m = st.m[sq], L = m + st.T[sq];
+    for (int64_t q0 = 0; q0 < L; q0 += 2 * BM) {
+      const int64_t i_hi = std::min(q0 + 2 * BM - 1, L - 1);
+      const int64_t np = std::min((m + BN - 1) / BN, i_hi / BN + 1);
+      const int64_t i_lo = std::max(q0, m);
+      int64_t nb = 0;
+      if (i_lo <= i_hi) {
+        const int64_t band_lo = std::max(m, i_lo - n + 1);
+        const int64_t kb = std::max(band_lo / BN, np);
+        nb = std::max<int64_t>(0, i_hi / BN - kb + 1);
+      }
+      total += np + nb;
+    }
+  }
+  return total;
+}
+
 bool prefill_tc_supported(const CacheView& cv) {
   return cv.dtype == RSWA_BF16 && cv.d == HD && encode_fn() != nullptr;
 }
@@ -506,8 +621,12 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
       !make_map(&mv, V, cv.Hkv, end_row))
     return cudaErrorInvalidValue;
   // Per device (the attribute belongs to the current device's context).
-  cudaError_t e = cudaFuncSetAttribute(
-      prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_tc_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   // Work units are pairs of 128-row tiles: tile_off counts pairs here.
   SeqTable st = st_in;
@@ -519,10 +638,28 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
     st.tile_off[i + 1] = pairs;
   }
   if (pairs == 0) return cudaSuccess;
-  const int64_t grid = (int64_t)pairs * cv.H;
-  if (grid >= (int64_t(1) << 31)) return cudaErrorNotSupported;
-  prefill_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-      mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
+  const int64_t units = (int64_t)pairs * cv.H;
+  if (units >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  // One CTA per SM fits (shared memory, 512 TMEM columns).  Units of few key
+  // tiles (band-dominated sequences) run persistently, one unit per round of
+  // gridDim units, so that the next unit's loads overlap this one's tail;
+  // long units run one per CTA, left to the hardware's dynamic scheduling.
+  int64_t grid = units;
+  const bool persist = host_tiles(st, cv.n) < kPersistentTilesPerUnit * pairs;
+  if (persist) {
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    grid = std::min<int64_t>(units, std::max(sms, 1));
+  }
+  if (persist)
+    prefill_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
+  else
+    prefill_tc_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
   return cudaGetLastError();
 }
 

@@ -182,7 +182,8 @@ DECODE_CASES = [
     ([300], 2048, 200, 2, 128),   # n >= T: the full-cache (MHA) baseline
     ([64], 512, 300, 2, 128),     # n >= T on the cluster path
     # more than 152 heads in flight: the split-K kernel with its global combine
-    ([37 * (i % 7) + 3 for i in range(20)], 16, 12, 8, 128),
+    # (m_b = 0 sequences have a single chunk and skip the combine)
+    ([0 if i % 4 == 0 else 37 * (i % 7) + 3 for i in range(20)], 16, 12, 8, 128),
 ]
 
 
