@@ -1027,6 +1027,16 @@ def main_only(args):
 
         def step():
             st["cache"].decode_step_fused(q, k, v, o, stream=s)
+    elif args.only == "vanilla_prefill":
+        import sliding_window_attention_02_gb300 as rswa
+        import workloads
+        H, d, n, L = 10, 128, 128, 32768        # m = 0: band tiles only
+        Q, K, V = workloads.qkv(L, H, d, 100, 1.0, torch.bfloat16, device=dev)
+        c = rswa.RswaCache(0, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+        O = torch.empty(L, H, d, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            c.prefill(Q, K, V, O, [0], L, stream=s)
     else:
         pf = setup_prefill(dev, layers=args.layers)
         w = pf["w"]
@@ -1067,7 +1077,8 @@ def main():
     ap.add_argument("--cpu-configs-worker", action="store_true")
     ap.add_argument("--cpu-max-steps", type=int, default=None)
     ap.add_argument("--only", default=None,
-                    choices=["single_page", "batched", "sweep", "gqa", "prefill"],
+                    choices=["single_page", "batched", "sweep", "gqa", "prefill",
+                             "vanilla_prefill"],
                     help="run one workload warmup+steps times and print its "
                          "mean step time (for profiling)")
     ap.add_argument("--layers", type=int, default=None,
