@@ -178,6 +178,38 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t* r) {
 }
 
 
+// 32 columns of this warp's 32 lanes, asynchronous: r is valid only after
+// tmem_wait_ld32(r).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]),
+        "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Wait for this thread's outstanding TMEM loads.  r (the registers of the
+// last load) are in-out operands, so no use of them moves above the wait.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t* r) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+        "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+        "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]),
+        "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+        "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]),
+        "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -414,11 +446,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const int hi = i - k0;   // visible: c <= hi && (c < a || c > b)
         const int a = m - k0;
         const int b = i - n - k0;
+        // The load of chunk c + 1 is in flight while chunk c is reduced.
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t v[32];
-          tmem_ld32_sync(s_addr + c0, v);
+        uint32_t va[32], vb[32];
+        auto max_chunk = [&](uint32_t* v, int c0) {
           if (!full) {
             // Mask in place and write back, so pass 2 reads masked logits.
 #pragma unroll
@@ -435,7 +466,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
             mx[2] = fmax3(mx[2], __uint_as_float(v[e + 4]), __uint_as_float(v[e + 5]));
             mx[3] = fmax3(mx[3], __uint_as_float(v[e + 6]), __uint_as_float(v[e + 7]));
           }
-        }
+        };
+        tmem_ld32(s_addr, va);
+        tmem_wait_ld32(va);
+        tmem_ld32(s_addr + 32, vb);
+        max_chunk(va, 0);
+        tmem_wait_ld32(vb);
+        tmem_ld32(s_addr + 64, va);
+        max_chunk(vb, 32);
+        tmem_wait_ld32(va);
+        tmem_ld32(s_addr + 96, vb);
+        max_chunk(va, 64);
+        tmem_wait_ld32(vb);
+        max_chunk(vb, 96);
         if (!full) tmem_wait_st();
         const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
         // Lazy rescale: keep the reference maximum unless it grew by > 2^8.
@@ -468,16 +511,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         // columns of S_h (two bf16 per column), 64 logits at a time.  Columns
         // 0..63 of S_h are read before any P column is written.
         uint32_t pk[2][32];
-        // Two logits per packed f32x2 FMA and sum.
+        // Two logits per packed f32x2 FMA and sum; the load of chunk c + 1
+        // is in flight while chunk c is exponentiated.
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(nref, nref);
         uint64_t ps2[2] = {0, 0};
+        auto exp_chunk = [&](const uint32_t* v, uint32_t* out) {
 #pragma unroll
-        for (int hc = 0; hc < 2; ++hc) {
-          uint32_t v[64];
-          tmem_ld32_sync(s_addr + 64 * hc, v);
-          tmem_ld32_sync(s_addr + 64 * hc + 32, v + 32);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
+          for (int c = 0; c < 16; ++c) {
             const int e = 2 * c;
             float x0, x1;
             f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
@@ -485,9 +525,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       x0, x1);
             const float p0 = ex2(x0), p1 = ex2(x1);
             ps2[c & 1] = f2_add(ps2[c & 1], f2_pack(p0, p1));
-            pk[hc][c] = pack_bf16(p0, p1);
+            out[c] = pack_bf16(p0, p1);
           }
-        }
+        };
+        tmem_ld32(s_addr, va);
+        tmem_wait_ld32(va);
+        tmem_ld32(s_addr + 32, vb);
+        exp_chunk(va, pk[0]);
+        tmem_wait_ld32(vb);
+        tmem_ld32(s_addr + 64, va);
+        exp_chunk(vb, pk[0] + 16);
+        tmem_wait_ld32(va);
+        tmem_ld32(s_addr + 96, vb);
+        exp_chunk(va, pk[1]);
+        tmem_wait_ld32(vb);
+        exp_chunk(vb, pk[1] + 16);
         float s0, s1, s2, s3;
         f2_unpack(ps2[0], s0, s1);
         f2_unpack(ps2[1], s2, s3);

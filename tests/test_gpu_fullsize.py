@@ -139,3 +139,66 @@ def test_multipage_prefill_full(cuda_lib):
     check(f64(O[rows]), ref, "multipage rows")
     assert cache.get_t(0) == T
     assert cache.cache_len(0) == m + n
+
+
+def _sample_rows(L, tile_edges, rng, extra=24):
+    rows = set(x for x in tile_edges if 0 <= x < L)
+    rows.update(rng.integers(0, L, extra).tolist())
+    return sorted(rows)
+
+
+def test_vanilla_swa_prefill_full(cuda_lib):
+    """m = 0, n = 128, 32K rows, 10 heads, as bench.py's vanilla SWA prefill:
+    1280 units of 3 key tiles run persistently, 8-9 units per CTA, so every
+    cross-unit phase (Q reload, O hand-over) is exercised many times."""
+    import workloads
+    rswa = cuda_lib
+    dev = torch.device("cuda", 0)
+    H, d, n, L = 10, 128, 128, 32768
+    Q, K, V = workloads.qkv(L, H, d, 100, 1.0, torch.bfloat16, device=dev)
+    cache = rswa.RswaCache(0, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+    O = torch.empty(L, H, d, dtype=torch.bfloat16, device=dev)
+    cache.prefill(Q, K, V, O, [0], L)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    rng = np.random.default_rng(1)
+    edges = [0, 1, 126, 127, 128, 129, 255, 256, 257, 383, 384, 511, 512,
+             152 * 256 - 1, 152 * 256, 152 * 256 + 130, L - 257, L - 129, L - 1]
+    rows = _sample_rows(L, edges, rng)
+    ref, _ = oracle.prefill_attention(f64(Q), f64(K), f64(V), 0, n, rows=rows)
+    check(f64(O[rows]), ref, "vanilla SWA rows")
+    assert cache.get_t(0) == L
+    assert cache.cache_len(0) == n
+
+
+def test_varlen_prefill_persistent_rounds(cuda_lib):
+    """Packed sequences with short prefixes (units of 3-11 key tiles, mixed
+    prefix, diagonal and band tiles): 510 units over one CTA per SM, so CTAs
+    cross sequences and unit shapes from one round to the next."""
+    import workloads
+    rswa = cuda_lib
+    dev = torch.device("cuda", 0)
+    H, d, n = 10, 128, 128
+    m_list = [0, 300, 77, 1000, 5]
+    t_list = [3000, 2500, 4000, 1200, 700]
+    rows_total = sum(m + t for m, t in zip(m_list, t_list))
+    Q, K, V = workloads.qkv(rows_total, H, d, 55, 1.0, torch.bfloat16, device=dev)
+    cache = rswa.RswaCache(max(m_list), n, H, d, len(m_list), rswa.RSWA_BF16,
+                           device=dev)
+    O = torch.empty_like(Q)
+    cache.prefill_varlen(Q, K, V, O, m_list, t_list)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    rng = np.random.default_rng(2)
+    off = 0
+    for b, (m, T) in enumerate(zip(m_list, t_list)):
+        L = m + T
+        edges = [0, 1, 127, 128, 255, 256, m - 1, m, m + 1, m + 127, m + 128,
+                 m + 255, m + 256, L - 129, L - 128, L - 1]
+        rows = _sample_rows(L, edges, rng, extra=12)
+        sl = slice(off, off + L)
+        ref, _ = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m,
+                                          n, rows=rows)
+        check(f64(O[sl][rows]), ref, f"seq {b} (m {m}, T {T})")
+        assert cache.get_t(b) == T
+        off += L
