@@ -552,7 +552,7 @@ cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
   const bool pf = prefetch_prefix;
   if (cv.H != cv.Hkv && !decode_use_small(cv)) {
     if (RSWA_GQA_TC && gqa_tc_supported(cv))
-      return launch_decode_gqa_tc(cv, q, k, v, o, lse, fused, s);
+      return launch_decode_gqa_tc(cv, q, k, v, o, lse, fused, pf, s);
     if (decode_gqa_heads_per_cta(cv) > 1)
       return launch_decode_gqa(cv, q, k, v, o, lse, fused, s);
   }

@@ -51,6 +51,7 @@ constexpr int kProducerWarp = 4, kMmaWarp = 5;
 #define RSWA_TC_STAGES 3
 #endif
 constexpr int NS = RSWA_TC_STAGES;          // ring slots (a K or a V tile)
+static_assert(NS >= 2, "a chunk's first K and V tiles take slots 0 and 1");
 constexpr uint32_t kSub = BN * 64 * 2;      // [128][64] bf16, 128B-swizzled
 constexpr uint32_t kTileB = 2 * kSub;       // [128][128] bf16 = 32 KB
 constexpr uint32_t kNAtom = NQ * 128;       // [16][64] bf16 atom = 2 KB
@@ -85,7 +86,10 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
          ((uint32_t)(((cc * 2) >> 4) ^ (r & 7)) << 4) + (uint32_t)((cc * 2) & 15);
 }
 
-template <bool FUSED, int G>
+// PREFETCH: the preceding kernel of the stream writes no prefix row, so a
+// prefix slot's first K and V tiles may be requested before the dependency
+// wait.
+template <bool FUSED, int G, bool PREFETCH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, CacheView cv,
@@ -122,7 +126,31 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     tmem_relinquish();
   }
   __syncthreads();                                  // barriers initialised
+  // A prefix slot's first K and V tiles start at slab row y * chunk whatever
+  // m_b is: request them (ring slots 0 and 1, loads 0 and 1 of the chunk)
+  // before the state loads.  A slot past this sequence's prefix drains them
+  // unused.
+  const int chunk = cv.chunk;
+  const int cp_cap = (int)((cv.m_cap + chunk - 1) / chunk);
+  const int y = blockIdx.y;
+  const size_t bkv = (size_t)b * cv.Hkv + kv;
+  const bool spec = y < cp_cap;
+  auto spec_loads = [&]() {
+    if (warp == kProducerWarp && lane == 0 && spec) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int yr = (int)((int64_t)bkv * cv.slab_rows + (int64_t)y * chunk);
+      mbar_arrive_expect_tx(bar(B_FULL + 0), kTileB);
+      tma_load_2d(sb + OFF_RING, &tmK, 0, yr, bar(B_FULL + 0));
+      tma_load_2d(sb + OFF_RING + kSub, &tmK, 64, yr, bar(B_FULL + 0));
+      mbar_arrive_expect_tx(bar(B_FULL + 1), kTileB);
+      tma_load_2d(sb + OFF_RING + kTileB, &tmV, 0, yr, bar(B_FULL + 1));
+      tma_load_2d(sb + OFF_RING + kTileB + kSub, &tmV, 64, yr, bar(B_FULL + 1));
+    }
+  };
+  if (PREFETCH) spec_loads();
   griddep_wait();
+  if (!PREFETCH) spec_loads();
 
   // The query rows of the KV head's heads (column tid), loaded alongside the
   // state words: their address does not depend on them.
@@ -136,7 +164,6 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 
   // This chunk: slab rows [j0, j1) of KV head (b, kv).
   const int64_t m_b = cv.m_dev[b];
-  const int chunk = cv.chunk;
   const int cp = (int)((m_b + chunk - 1) / chunk);
   const int nch = cp + (int)((cv.n + chunk - 1) / chunk);
   // Grid slot y: prefix chunk y while y < ceil(m_cap / chunk) (no work past
@@ -144,12 +171,9 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   // launch in order, so every sequence's prefix chunks run before the
   // one-tile ring chunks, which fill the last wave.  c is the chunk's index
   // among this sequence's nch partials.
-  const int cp_cap = (int)((cv.m_cap + chunk - 1) / chunk);
-  const int y = blockIdx.y;
   const bool live = y >= cp_cap || y < cp;
   const int c = y < cp_cap ? y : cp + (y - cp_cap);
   const size_t bh0 = (size_t)b * cv.H + (size_t)kv * per_kv;
-  const size_t bkv = (size_t)b * cv.Hkv + kv;
   const int64_t t_b = cv.t_dev[bh0];                // equal for the heads
   int64_t j0 = 0, j1 = 0, sub = -1;
   if (live) {
@@ -199,7 +223,9 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     if (lane == 0 && live) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      for (int idx = 0; idx < first_loads; ++idx) load(idx);
+      // A live prefix chunk starts at slab row y * chunk: its loads 0 and 1
+      // are the ones requested above.
+      for (int idx = spec ? 2 : 0; idx < first_loads; ++idx) load(idx);
     }
   } else if (tid < kSoftThreads) {
     // Q_G^T as the MMA's B operand: row g = query head g, K-major over d.
@@ -237,6 +263,10 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       // Drain: every copy issued has landed before the CTA may exit.
       for (int idx = max(0, issued - NS); idx < issued; ++idx)
         mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, never, kWaitLimitNs);
+    } else if (lane == 0 && spec) {
+      // A prefix slot past this sequence's prefix: its two early loads.
+      mbar_wait(bar(B_FULL + 0), 0, never, kWaitLimitNs);
+      mbar_wait(bar(B_FULL + 1), 0, never, kWaitLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -456,11 +486,11 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   if (tid == 0 && *abort_flag) flag_error(cv.err, kErrWaitTimeout);
 }
 
-template <bool FUSED, int G>
+template <bool FUSED, int G, bool PREFETCH>
 cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
                       const CUtensorMap& mv, const void* q, const void* k,
                       const void* v, void* o, float* lse, cudaStream_t s) {
-  auto kern = decode_gqa_tc_kernel<FUSED, G>;
+  auto kern = decode_gqa_tc_kernel<FUSED, G, PREFETCH>;
   // Per device (the attribute belongs to the current device's context).
   cudaError_t e = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -481,15 +511,15 @@ cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
                             (const BF*)(FUSED ? v : nullptr), (BF*)o, lse);
 }
 
-template <bool FUSED>
+template <bool FUSED, bool PREFETCH>
 cudaError_t launch_tc_g(const CacheView& cv, const CUtensorMap& mk,
                         const CUtensorMap& mv, const void* q, const void* k,
                         const void* v, void* o, float* lse, cudaStream_t s) {
   const int per_kv = cv.H / cv.Hkv;
-  if (per_kv <= 2) return launch_tc<FUSED, 2>(cv, mk, mv, q, k, v, o, lse, s);
-  if (per_kv <= 4) return launch_tc<FUSED, 4>(cv, mk, mv, q, k, v, o, lse, s);
-  if (per_kv <= 8) return launch_tc<FUSED, 8>(cv, mk, mv, q, k, v, o, lse, s);
-  return launch_tc<FUSED, 16>(cv, mk, mv, q, k, v, o, lse, s);
+  if (per_kv <= 2) return launch_tc<FUSED, 2, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
+  if (per_kv <= 4) return launch_tc<FUSED, 4, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
+  if (per_kv <= 8) return launch_tc<FUSED, 8, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
+  return launch_tc<FUSED, 16, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
 }
 
 }  // namespace
@@ -503,14 +533,20 @@ bool gqa_tc_supported(const CacheView& cv) {
 
 cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,
                                  const void* k, const void* v, void* o,
-                                 float* lse, bool fused, cudaStream_t s) {
+                                 float* lse, bool fused, bool prefetch_prefix,
+                                 cudaStream_t s) {
   const uint64_t rows = (uint64_t)cv.B * cv.Hkv * cv.slab_rows;
   CUtensorMap mk, mv;
   if (!make_tmap_rows_bf16(&mk, cv.K, HD, rows) ||
       !make_tmap_rows_bf16(&mv, cv.V, HD, rows))
     return cudaErrorInvalidValue;
-  cudaError_t e = fused ? launch_tc_g<true>(cv, mk, mv, q, k, v, o, lse, s)
-                        : launch_tc_g<false>(cv, mk, mv, q, k, v, o, lse, s);
+  cudaError_t e;
+  if (prefetch_prefix)
+    e = fused ? launch_tc_g<true, true>(cv, mk, mv, q, k, v, o, lse, s)
+              : launch_tc_g<false, true>(cv, mk, mv, q, k, v, o, lse, s);
+  else
+    e = fused ? launch_tc_g<true, false>(cv, mk, mv, q, k, v, o, lse, s)
+              : launch_tc_g<false, false>(cv, mk, mv, q, k, v, o, lse, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -76,9 +76,12 @@ inline bool gqa_tc_shape(int heads, int kv_heads, int head_dim, int dtype) {
   return dtype == RSWA_BF16 && head_dim == 128 && per_kv >= 2 && per_kv <= 16;
 }
 bool gqa_tc_supported(const CacheView& cv);
+// prefetch_prefix: the stream's preceding kernel writes no prefix row of
+// this cache (the first K/V tiles of prefix chunks load before its end).
 cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,
                                  const void* k, const void* v, void* o,
-                                 float* lse, bool fused, cudaStream_t s);
+                                 float* lse, bool fused, bool prefetch_prefix,
+                                 cudaStream_t s);
 // [rows][cols] bf16, row-major, as a 2-D TMA map: box 64 columns x 128 rows,
 // 128-byte swizzle; rows past `rows` read as zero.
 bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
