@@ -561,6 +561,40 @@ def test_gqa_decode_tc_multitile(cuda_lib):
         assert cache.get_t(b) == T
 
 
+def test_gqa_decode_tc_wrapped_two_tile_ring(cuda_lib):
+    """A two-tile ring (n = 256) that has wrapped (T = 300 outputs prefilled,
+    so slot j mod n holds output j for j = 44 .. 299) behind multi-tile
+    512-key prefix chunks; each fused step's new key and value land in a
+    slot of the ring chunk's second or first tile.  Three fused steps must
+    match the oracle rows m + 300 .. m + 302."""
+    rswa = cuda_lib
+    B, H, Hkv, d, n, T0, steps = 24, 32, 8, 128, 256, 300, 3
+    m_list = [600 + 13 * b for b in range(B)]       # last chunk 1..3 tiles
+    L = [m + T0 + steps for m in m_list]
+    Q, K, V = _qkv_gqa(sum(L), H, Hkv, d, seed=61)
+    offs = np.cumsum([0] + L)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    pk = torch.cat([K[offs[b]:offs[b] + m_list[b] + T0] for b in range(B)]).cuda()
+    pv = torch.cat([V[offs[b]:offs[b] + m_list[b] + T0] for b in range(B)]).cuda()
+    cache.prefill_varlen(None, pk, pv, None, m_list, [T0] * B)
+    got = np.zeros((steps, B, H, d))
+    for t in range(steps):
+        r = [offs[b] + m_list[b] + T0 + t for b in range(B)]
+        q, k, v = (x[r].contiguous().cuda() for x in (Q, K, V))
+        o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+        cache.decode_step_fused(q, k, v, o)
+        got[t] = f64(o)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b in [0, 5, 9, 10, 14, 23]:
+        m = m_list[b]
+        sl = slice(offs[b], offs[b] + L[b])
+        ref, _ = oracle.prefill_attention(f64(Q[sl]), f64(K[sl]), f64(V[sl]), m, n,
+                                          rows=list(range(m + T0, m + T0 + steps)))
+        assert_close(got[:, b], ref, 1, f"seq {b} (m {m})")
+        assert cache.get_t(b) == T0 + steps
+
+
 @pytest.mark.parametrize("dtype", [1, 0], ids=["bf16-tc", "f32"])
 def test_gqa_decode_empty_ring(cuda_lib, dtype):
     """decode_step right after a prefix-only prefill (t_b = 0, nothing
