@@ -22,13 +22,15 @@ namespace rswa {
 // m_b of this cache (the host's per-handle flag), so a prefix-chunk CTA
 // reads m_b and loads its warps' first row batch before the dependency
 // wait, while the previous kernel drains.
-template <typename T, int D, bool FUSED, bool PREFETCH>
-__global__ void __launch_bounds__(kDecodeThreads, 5)
+// NW warps per CTA: 4 (five CTAs per SM) in general; 8 when the grid is
+// small enough to stay in one wave, so that each CTA takes half as many
+// dependent row batches.
+template <typename T, int D, bool FUSED, bool PREFETCH, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 5 : 2)
 decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
               const T* __restrict__ vnew, T* __restrict__ o,
               float* __restrict__ lse) {
   using C = AttendCfg<T, D>;
-  constexpr int NW = kDecodeThreads / 32;
   const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = cv.H / cv.Hkv;                  // query heads per KV head
@@ -493,6 +495,36 @@ static cudaError_t launch_cluster(const CacheView& cv, const T* q, const T* k,
                     grid, block, cl, s, cv, q, k, v, o, lse);
 }
 
+// bf16 split-K CTAs get 8 warps (two resident per SM) when the whole grid
+// fits one wave of them; otherwise 4 warps (five per SM).  Measured on the
+// one-sequence, 12-layer workload: a 4-page prefix (100 CTAs) 6.18 -> 5.5 us
+// per layer with 8 warps; 16 and 40 pages (340 and 420 CTAs) lose a wave and
+// slow down with them.
+constexpr int64_t kWideDecodeCtas = 152 * 2;
+
+template <typename T, int D, int NW>
+static cudaError_t launch_split(const CacheView& cv, const T* qq, const T* kk,
+                                const T* vv, T* oo, float* lse, bool fused,
+                                bool prefetch, cudaStream_t s) {
+  const dim3 grid(cv.max_chunks, cv.H, cv.B), block(NW * 32);
+  const T* nk = nullptr;
+  // The preloaded batch costs registers: bf16 caches only (float32 ones
+  // would spill).
+  if constexpr (sizeof(T) == 2) {
+    if (fused && prefetch)
+      return launch_pdl(decode_kernel<T, D, true, true, NW>, grid, block, 0, s, cv,
+                        qq, kk, vv, oo, lse);
+    if (prefetch)
+      return launch_pdl(decode_kernel<T, D, false, true, NW>, grid, block, 0, s, cv,
+                        qq, nk, nk, oo, lse);
+  }
+  if (fused)
+    return launch_pdl(decode_kernel<T, D, true, false, NW>, grid, block, 0, s, cv, qq,
+                      kk, vv, oo, lse);
+  return launch_pdl(decode_kernel<T, D, false, false, NW>, grid, block, 0, s, cv, qq,
+                    nk, nk, oo, lse);
+}
+
 template <typename T, int D>
 static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
                                    const void* k, const void* v, void* o,
@@ -509,24 +541,13 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
     else
       e = launch_cluster<T, D, false>(cv, qq, nullptr, nullptr, oo, lse,
                                       prefetch, s);
-  } else {
-    const dim3 grid(cv.max_chunks, cv.H, cv.B), block(kDecodeThreads);
-    const T* nk = nullptr;
-    // The preloaded batch costs registers: bf16 caches only (float32 ones
-    // would spill).
-    prefetch = prefetch && sizeof(T) == 2;
-    if (fused && prefetch)
-      e = launch_pdl(decode_kernel<T, D, true, true>, grid, block, 0, s, cv, qq, kk,
-                     vv, oo, lse);
-    else if (fused)
-      e = launch_pdl(decode_kernel<T, D, true, false>, grid, block, 0, s, cv, qq, kk,
-                     vv, oo, lse);
-    else if (prefetch)
-      e = launch_pdl(decode_kernel<T, D, false, true>, grid, block, 0, s, cv, qq, nk,
-                     nk, oo, lse);
+  } else if constexpr (sizeof(T) == 2) {
+    if ((int64_t)cv.B * cv.H * cv.max_chunks <= kWideDecodeCtas)
+      e = launch_split<T, D, 8>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
     else
-      e = launch_pdl(decode_kernel<T, D, false, false>, grid, block, 0, s, cv, qq, nk,
-                     nk, oo, lse);
+      e = launch_split<T, D, 4>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
+  } else {
+    e = launch_split<T, D, 4>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
