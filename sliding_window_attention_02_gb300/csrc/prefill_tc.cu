@@ -112,6 +112,23 @@ __device__ __forceinline__ int tile_at(const TileRange& t, int j) {
   return j < t.np ? j : t.kb_start + (j - t.np);
 }
 
+// Whether key tile k0 .. k0+BN-1 holds a key that some row of the 128-row
+// query tile at qh sees (sequence with prefix m, window n, length L).
+// Prefix keys are seen by every output row and causally by prefix rows;
+// keys at or past m only by output rows i with i - n + 1 <= key <= i, of
+// which the first output row reaches furthest back.  A (query tile, key
+// tile) product that fails this is skipped: both tiles of a unit walk the
+// union of their key tiles, and e.g. a band-only unit has two such
+// products out of six (the persistent form skips them).
+__device__ __forceinline__ bool tile_touches(int k0, int qh, int m, int n, int L) {
+  const int i_hi = min(qh + BM - 1, L - 1);     // last row of the tile
+  if (k0 > i_hi) return false;                  // above the diagonal
+  if (k0 < m) return true;                      // prefix keys, k0 <= i_hi
+  const int i_lo = max(qh, m);                  // first output row
+  if (i_lo > i_hi) return false;                // prefix rows only
+  return k0 + BN - 1 >= i_lo - n + 1;
+}
+
 // The k-th unit of CTA b out of G: rounds of G units, walked forward in even
 // rounds and backward in odd ones, so that with units in heavy-first order
 // every CTA's sum of work is near the mean (as list scheduling would give,
@@ -229,9 +246,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// PERSIST: a CTA may take several units (one per round of gridDim units);
-// otherwise exactly one, unit blockIdx.x, and the cross-unit barriers
-// (B_QFREE, B_OFREE) and phase counters fold away.
+// PERSIST: a CTA may take several units (one per round of gridDim units)
+// and skips (query tile, key tile) products the mask excludes entirely;
+// otherwise exactly one unit, blockIdx.x, the cross-unit barriers (B_QFREE,
+// B_OFREE) and phase counters fold away, and every product of the unit's
+// tile list runs.
 template <bool PERSIST>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -349,6 +368,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                       desc_sw128(vb + k * 2048, kSub, 1024), idesc_pv,
                       (acc || k > 0) ? 1u : 0u);
       };
+      const int nwin = (int)min(cv.n, (int64_t)1 << 30);
       uint32_t gi = 0, gt = 0, kq = 0;          // loads, tiles, units done
       bool ok = true;
       for (int k = 0, u; ok && k < kMaxRounds && (u = snake_unit(k, blockIdx.x, gridDim.x, units)) >= 0;
@@ -358,46 +378,113 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (nt == 0) continue;
         if (!wait(B_Q, kq) || !wait_slot(gi)) break;
         tc_fence_after();
-        qk(0, gi);
-        qk(1, gi);
-        mma_commit(bar(B_EMPTY + gi % NS));
-        if (nt == 1) mma_commit(bar(B_QFREE));
-        for (int j = 0; j < nt; ++j) {
-          const uint32_t vi = gi + 2 * j + 1, ki = gi + 2 * j + 2;
-          const bool more = j + 1 < nt;
-          // PV_h of the unit's first tile overwrites O_h: the previous
-          // unit's epilogue must have read it.
-          if (!wait(B_P + 0, gt + j) || !wait_slot(vi) ||
-              (j == 0 && kq > 0 && !wait(B_OFREE + 0, kq - 1))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          pv(0, vi, j > 0);
-          if (more) {
-            if (!wait_slot(ki)) {
+        if constexpr (!PERSIST) {
+          // Long units: every product of the unit's tile list runs.  (This
+          // issuing thread sits on the critical path: a per-tile skip test
+          // here measured 1-6 % slower on the multi-page prefill.)
+          qk(0, gi);
+          qk(1, gi);
+          mma_commit(bar(B_EMPTY + gi % NS));
+          if (nt == 1) mma_commit(bar(B_QFREE));
+          for (int j = 0; j < nt; ++j) {
+            const uint32_t vi = gi + 2 * j + 1, ki = gi + 2 * j + 2;
+            const bool more = j + 1 < nt;
+            if (!wait(B_P + 0, gt + j) || !wait_slot(vi)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            qk(0, ki);
-          } else {
-            mma_commit(bar(B_O + 0));
+            pv(0, vi, j > 0);
+            if (more) {
+              if (!wait_slot(ki)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              qk(0, ki);
+            } else {
+              mma_commit(bar(B_O + 0));
+            }
+            if (!wait(B_P + 1, gt + j)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv(1, vi, j > 0);
+            mma_commit(bar(B_EMPTY + vi % NS));
+            if (more) {
+              qk(1, ki);
+              mma_commit(bar(B_EMPTY + ki % NS));
+              if (j + 2 == nt) mma_commit(bar(B_QFREE));   // last QK of the unit
+            } else {
+              mma_commit(bar(B_O + 1));
+            }
           }
-          if (!wait(B_P + 1, gt + j) ||
-              (j == 0 && kq > 0 && !wait(B_OFREE + 1, kq - 1))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          pv(1, vi, j > 0);
-          mma_commit(bar(B_EMPTY + vi % NS));
-          if (more) {
-            qk(1, ki);
-            mma_commit(bar(B_EMPTY + ki % NS));
-            if (j + 2 == nt) mma_commit(bar(B_QFREE));   // last QK of the unit
-          } else {
-            mma_commit(bar(B_O + 1));
+        } else {
+          // Short units: products the mask excludes entirely are skipped.
+          // A skipped QK still completes S_h's barrier (the softmax warps
+          // hand P_h back at once); the unit's first PV of a half that runs
+          // overwrites O_h.
+          auto use = [&](int half, int j) {
+            return tile_touches(tile_at(w.tr, j) * BN, w.q0 + half * BM, w.m, nwin, w.L);
+          };
+          bool pv_done[2] = {false, false};
+          auto qk_if = [&](int half, uint32_t g, bool on) {
+            if (on)
+              qk(half, g);
+            else
+              mma_commit(bar(B_S + half));
+          };
+          auto pv_if = [&](int half, uint32_t g, bool on) {
+            if (!on) return;
+            pv(half, g, pv_done[half]);
+            pv_done[half] = true;
+          };
+          bool u0 = use(0, 0), u1 = use(1, 0);
+          qk_if(0, gi, u0);
+          qk_if(1, gi, u1);
+          mma_commit(bar(B_EMPTY + gi % NS));
+          if (nt == 1) mma_commit(bar(B_QFREE));
+          for (int j = 0; j < nt; ++j) {
+            const uint32_t vi = gi + 2 * j + 1, ki = gi + 2 * j + 2;
+            const bool more = j + 1 < nt;
+            const bool n0 = more && use(0, j + 1), n1 = more && use(1, j + 1);
+            // PV_h of the unit's first tile overwrites O_h: the previous
+            // unit's epilogue must have read it.
+            if (!wait(B_P + 0, gt + j) || !wait_slot(vi) ||
+                (j == 0 && kq > 0 && !wait(B_OFREE + 0, kq - 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv_if(0, vi, u0);
+            if (more) {
+              if (!wait_slot(ki)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              qk_if(0, ki, n0);
+            } else {
+              mma_commit(bar(B_O + 0));
+            }
+            if (!wait(B_P + 1, gt + j) ||
+                (j == 0 && kq > 0 && !wait(B_OFREE + 1, kq - 1))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv_if(1, vi, u1);
+            mma_commit(bar(B_EMPTY + vi % NS));
+            if (more) {
+              qk_if(1, ki, n1);
+              mma_commit(bar(B_EMPTY + ki % NS));
+              if (j + 2 == nt) mma_commit(bar(B_QFREE));   // last QK of the unit
+            } else {
+              mma_commit(bar(B_O + 1));
+            }
+            u0 = n0;
+            u1 = n1;
           }
         }
         gi += 2 * nt;
@@ -442,6 +529,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           break;
         }
         tc_fence_after();
+        if (PERSIST && !tile_touches(k0, qh, m, n, w.L)) {
+          // No MMA wrote S_h for this tile: P_h is "ready" at once.
+          tc_fence_before();
+          mbar_arrive(bar(B_P + half));
+          continue;
+        }
         // Pass 1: row maximum over the visible logits, 32 columns at a time.
         const int hi = i - k0;   // visible: c <= hi && (c < a || c > b)
         const int a = m - k0;
