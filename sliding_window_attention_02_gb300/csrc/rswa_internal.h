@@ -10,7 +10,7 @@
 namespace rswa {
 
 constexpr int kMaxSeqPerLaunch = 128;   // sequences per prefill launch
-constexpr int kDecodeThreads = 128;     // threads per decode CTA
+constexpr int kDecodeThreads = 128;     // threads per grouped split-K decode CTA
 
 // Device view of a cache buffer.  All regions live in the caller's buffer.
 // H query heads share Hkv key/value heads (H % Hkv == 0): query head h reads
