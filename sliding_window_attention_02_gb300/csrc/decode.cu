@@ -52,8 +52,11 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     }
   }
   // Launched as a programmatic dependent: wait until the previous kernel in
-  // the stream has completed and its writes are visible.
+  // the stream has completed and its writes are visible.  The next step's
+  // CTAs may then take SM slots as this grid's CTAs finish; they wait for
+  // this grid.
   griddep_wait();
+  griddep_launch_dependents();
 
   if (!PREFETCH) m_b = cv.m_dev[b];
   const int chunk = cv.chunk;
@@ -108,8 +111,6 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   }
   attend_range<T, D>(qf, Kb, Vb, D, j0, j1, first, (int64_t)NW * C::KEYS_WARP, sub,
                      kn, vn, lane, st);
-  // The next step's kernel may start launching; it waits for this one.
-  griddep_launch_dependents();
   merge_groups<T, D>(st);
 
   // Merge the warps through shared memory.

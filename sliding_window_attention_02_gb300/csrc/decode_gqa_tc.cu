@@ -150,6 +150,9 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   };
   if (PREFETCH) spec_loads();
   griddep_wait();
+  // The next step's CTAs may take SM slots as this grid's CTAs finish (and
+  // do their set-up and early tile requests there); they wait for this grid.
+  griddep_launch_dependents();
   if (!PREFETCH) spec_loads();
 
   // The query rows of the KV head's heads (column tid), loaded alongside the
@@ -435,7 +438,6 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       if (lane == 0) red_sum[warp * NQ + g] = v;
     }
   }
-  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   if (live && tid < kSoftThreads) {
