@@ -16,7 +16,9 @@
  * Readings where the pages are silent: prefix rows attend causally among
  * themselves; the window of n includes the current token; the softmax scale
  * is 1/sqrt(head_dim); positions are applied by the caller (RoPE etc. before
- * Q/K reach this library); one KV head per query head.
+ * Q/K reach this library); one KV head per query head (standard MHA, the
+ * pages' baseline) unless the cache is created by rswa_cache_create_gqa,
+ * which lets several query heads share one KV head.
  *
  * Conventions shared by every call.
  *   - All device pointers are plain CUDA device addresses owned by the
@@ -244,8 +246,10 @@ RSWA_API int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
  *     bytes of counters, each rounded up to 256 bytes; a larger cache is
  *     rejected with RSWA_ECAPACITY before anything runs.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current).  Make that first call before
- *     any stream capture.
+ *     per device, with that device current) and keeps it for the life of
+ *     the process.  Make that first call before any stream capture, and do
+ *     not use this call across a device reset (cudaDeviceReset), which
+ *     reloads the library's device code and moves the array.
  *   - Every call shares the one array and it keeps the previous call's
  *     contents; each call clears its counters on the caller's stream first.
  *     Calls that overlap on the GPU (other streams, other caches, other

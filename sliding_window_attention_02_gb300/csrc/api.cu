@@ -68,6 +68,18 @@ struct DeviceGuard {
   }
 };
 
+// Runs a decode launch with the handle's permission to read prefix rows and
+// m_b before the dependency wait.  Only a launch that succeeded counts as the
+// decode launch that follows a prefill: when no kernel was launched, the next
+// decode call must still wait before it reads them.
+template <typename F>
+int run_decode(rswa_cache* cache, F launch) {
+  const bool prefetch = cache->prefix_stable.load();
+  const cudaError_t e = launch(prefetch);
+  if (e == cudaSuccess) cache->prefix_stable.store(true);
+  return status_of(e);
+}
+
 struct Layout {
   size_t m_off, t_off, err_off, k_off, v_off, part_off, cnt_bh_off;
   size_t total;
@@ -89,18 +101,22 @@ int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
 #define RSWA_DECODE_CTAS_PER_SM 32
 #endif
 
-// Keys per decode CTA, a power of two.  Many heads (more than the 152 SMs):
-// sized so that the largest possible decode grid holds about
-// RSWA_DECODE_CTAS_PER_SM CTAs per SM.  Few heads: about 40 chunks per head,
-// 128..256 keys each (measured best on GB300 for one sequence with a 1K-10K
-// key cache; shorter caches take the cluster path).
+// Keys per decode CTA, a power of two, for a device of `sms` SMs.  Many
+// heads (more than the SMs): sized so that the largest possible decode grid
+// holds about RSWA_DECODE_CTAS_PER_SM CTAs per SM.  Few heads: about 40
+// chunks per head, 128..256 keys each (measured best on GB300 for one
+// sequence with a 1K-10K key cache; shorter caches take the cluster path).
+// Never below kMinChunk, which bounds the split-K scratch.
 #ifndef RSWA_TC_WAVES
 #define RSWA_TC_WAVES 2
 #endif
 
+constexpr int kMinChunk = 64;
+
 int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
-                 int dtype, int batch) {
+                 int dtype, int batch, int sms) {
 #ifdef RSWA_DECODE_CHUNK
+  static_assert(RSWA_DECODE_CHUNK >= kMinChunk, "decode chunk");
   return RSWA_DECODE_CHUNK;
 #endif
   if (gqa_tc_shape(heads, kv_heads, head_dim, dtype)) {
@@ -108,13 +124,13 @@ int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
     // resident per SM; chunks are whole 128-key tiles, sized for about
     // RSWA_TC_WAVES waves of CTAs.
     const int64_t keys = (int64_t)batch * kv_heads * (m + n);
-    const int64_t target = 152 * 2 * RSWA_TC_WAVES;
+    const int64_t target = (int64_t)sms * 2 * RSWA_TC_WAVES;
     const int64_t want = (keys + target - 1) / target;
     int c = 128;
     while (c < want && c < 2048) c <<= 1;
     return c;
   }
-  if ((int64_t)batch * heads <= 152) {
+  if ((int64_t)batch * heads <= sms) {
     const int64_t want = (m + n + 39) / 40;
     int c = 128;
     while (c < want && c < 256) c <<= 1;
@@ -124,19 +140,26 @@ int choose_chunk(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
   // head once per group of query heads
   const int streams = heads / gqa_heads_per_cta(heads, kv_heads);
   const int64_t keys = (int64_t)batch * streams * (m + n);
-  const int64_t target = 152 * RSWA_DECODE_CTAS_PER_SM;
+  const int64_t target = (int64_t)sms * RSWA_DECODE_CTAS_PER_SM;
   int64_t want = (keys + target - 1) / target;
   int c = 64;
   while (c < want && c < 2048) c <<= 1;
   return c;
 }
 
+// Layout of a cache buffer.  The decode chunk depends on the device's SM
+// count (`sms`, 0 when no device is known: footprint queries); the split-K
+// scratch is sized for the smallest chunk, so the footprint is the same for
+// every device.
 Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
-                   int batch, int dtype) {
+                   int batch, int dtype, int sms) {
   Layout L{};
   const size_t elt = dtype == RSWA_F32 ? 4 : 2;
-  L.chunk = choose_chunk(m, n, heads, kv_heads, head_dim, dtype, batch);
+  L.chunk = sms > 0 ? choose_chunk(m, n, heads, kv_heads, head_dim, dtype, batch, sms)
+                    : kMinChunk;
   L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
+  const int64_t chunks_bound = (m + kMinChunk - 1) / kMinChunk +
+                               (n + kMinChunk - 1) / kMinChunk;
   size_t off = 0;
   L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);
   L.t_off = off;      off = align_up(off + sizeof(int64_t) * batch * heads);
@@ -149,7 +172,7 @@ Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
   L.v_off = off;
   off = align_up(off + elt * (size_t)batch * kv_heads * (size_t)(m + n) * head_dim);
   L.part_off = off;
-  off = align_up(off + sizeof(float) * (size_t)batch * heads * L.max_chunks *
+  off = align_up(off + sizeof(float) * (size_t)batch * heads * chunks_bound *
                            (head_dim + 2));
   L.total = off;
   return L;
@@ -180,7 +203,7 @@ int rswa_cache_footprint_gqa(int64_t m, int64_t n, int heads, int kv_heads,
   if (!out_bytes) return RSWA_EINVAL;
   const int st = valid_shape(m, n, heads, kv_heads, head_dim, batch, dtype);
   if (st != RSWA_OK) return st;
-  *out_bytes = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype).total;
+  *out_bytes = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype, 0).total;
   return RSWA_OK;
 }
 
@@ -206,11 +229,15 @@ int rswa_cache_create_gqa(int64_t m, int64_t n, int heads, int kv_heads,
   if (st != RSWA_OK) return st;
   if (!device_buf || (reinterpret_cast<uintptr_t>(device_buf) % kAlign) != 0)
     return RSWA_EINVAL;
-  const Layout L = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype);
-  if (buf_bytes < L.total) return RSWA_ECAPACITY;
+  if (buf_bytes < make_layout(m, n, heads, kv_heads, head_dim, batch, dtype, 0).total)
+    return RSWA_ECAPACITY;
   if (injected_failure()) return RSWA_ECUDA;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RSWA_ECUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    return RSWA_ECUDA;
+  const Layout L = make_layout(m, n, heads, kv_heads, head_dim, batch, dtype, sms);
 
   rswa_cache* c = new (std::nothrow) rswa_cache();
   if (!c) return RSWA_ECUDA;
@@ -233,6 +260,7 @@ int rswa_cache_create_gqa(int64_t m, int64_t n, int heads, int kv_heads,
   cv.slab_rows = m + n;
   cv.chunk = L.chunk;
   cv.max_chunks = L.max_chunks;
+  cv.sms = sms;
   c->device = dev;
   c->buf = device_buf;
   c->buf_bytes = buf_bytes;
@@ -348,9 +376,10 @@ int rswa_decode_step(rswa_cache* cache, const void* q, void* o, float* lse,
   if (injected_failure()) return RSWA_ECUDA;
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
-  return status_of(launch_decode(cache->cv, q, nullptr, nullptr, o, lse, false,
-                                 cache->prefix_stable.exchange(true),
-                                 static_cast<cudaStream_t>(stream)));
+  return run_decode(cache, [&](bool pf) {
+    return launch_decode(cache->cv, q, nullptr, nullptr, o, lse, false, pf,
+                         static_cast<cudaStream_t>(stream));
+  });
 }
 
 int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
@@ -361,9 +390,10 @@ int rswa_decode_step_fused(rswa_cache* cache, const void* q, const void* k,
   if (injected_failure()) return RSWA_ECUDA;
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
-  return status_of(launch_decode(cache->cv, q, k, v, o, lse, true,
-                                 cache->prefix_stable.exchange(true),
-                                 static_cast<cudaStream_t>(stream)));
+  return run_decode(cache, [&](bool pf) {
+    return launch_decode(cache->cv, q, k, v, o, lse, true, pf,
+                         static_cast<cudaStream_t>(stream));
+  });
 }
 
 int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
@@ -378,9 +408,10 @@ int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
   if (block == 1)  // [B][1][H][d] is the fused single step's [B][H][d]
-    return status_of(launch_decode(cache->cv, q, k, v, o, lse, true,
-                                   cache->prefix_stable.exchange(true),
-                                   static_cast<cudaStream_t>(stream)));
+    return run_decode(cache, [&](bool pf) {
+      return launch_decode(cache->cv, q, k, v, o, lse, true, pf,
+                           static_cast<cudaStream_t>(stream));
+    });
   return status_of(launch_decode_block(cache->cv, q, k, v, block, o, lse,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -398,10 +429,10 @@ int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,
   if (injected_failure()) return RSWA_ECUDA;
   DeviceGuard g(cache->device);
   if (!g.ok) return RSWA_ECUDA;
-  return status_of(launch_decode_fused_static(cache->cv, cache->device, q, k, v,
-                                              o, lse,
-                                              cache->prefix_stable.exchange(true),
-                                              static_cast<cudaStream_t>(stream)));
+  return run_decode(cache, [&](bool pf) {
+    return launch_decode_fused_static(cache->cv, cache->device, q, k, v, o, lse,
+                                      pf, static_cast<cudaStream_t>(stream));
+  });
 }
 
 static int read_state(rswa_cache* cache, int b, int64_t* m_b, int64_t* t_b) {

@@ -388,6 +388,11 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
       st_async_f32(map_dsmem(&c_ml[rank][1], 0), bar, Ls);
     }
   }
+  // Second phase of the cluster barrier: every thread arrives once it has
+  // issued its stores into rank 0.  Only rank 0's give-up path below waits
+  // on this phase; the partials themselves land on c_bar.
+  __syncwarp();
+  cluster_arrive_relaxed();
   if (rank != 0 || tid >= D) return;
   // Bounded wait for the CL partials; gives up at once when an earlier
   // launch on this cache already flagged an error.
@@ -399,6 +404,15 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
           (*(volatile int32_t*)cv.err != 0 ||
            ptx::globaltimer_ns() - t0 > kClusterWaitNs)) {
         flag_error(cv.err, kErrWaitTimeout);
+        // Giving up: this CTA must not exit while a peer may still store
+        // into its shared memory.  Wait until every thread of the cluster
+        // has issued its stores (arrived at the second phase) or exited -
+        // peers run straight-line code, so they all get there - then give
+        // the stores already issued a bounded time to land.
+        cluster_wait_divergent();
+        const uint64_t t1 = ptx::globaltimer_ns();
+        for (uint32_t it2 = 1; !ptx::mbar_try_wait(bar, 0); ++it2)
+          if ((it2 & 63u) == 0 && ptx::globaltimer_ns() - t1 > kClusterWaitNs) break;
         return;
       }
     }
@@ -497,11 +511,11 @@ static cudaError_t launch_cluster(const CacheView& cv, const T* q, const T* k,
 }
 
 // bf16 split-K CTAs get 8 warps (two resident per SM) when the whole grid
-// fits one wave of them; otherwise 4 warps (five per SM).  Measured on the
-// one-sequence, 12-layer workload: a 4-page prefix (100 CTAs) 6.18 -> 5.5 us
-// per layer with 8 warps; 16 and 40 pages (340 and 420 CTAs) lose a wave and
-// slow down with them.
-constexpr int64_t kWideDecodeCtas = 152 * 2;
+// fits one wave of them (2 x the SM count); otherwise 4 warps (five per SM).
+// Measured on the one-sequence, 12-layer workload on GB300 (152 SMs): a
+// 4-page prefix (100 CTAs) 6.18 -> 5.5 us per layer with 8 warps; 16 and 40
+// pages (340 and 420 CTAs) lose a wave and slow down with them.
+constexpr int64_t kWideCtasPerSm = 2;
 
 template <typename T, int D, int NW>
 static cudaError_t launch_split(const CacheView& cv, const T* qq, const T* kk,
@@ -543,7 +557,7 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
       e = launch_cluster<T, D, false>(cv, qq, nullptr, nullptr, oo, lse,
                                       prefetch, s);
   } else if constexpr (sizeof(T) == 2) {
-    if ((int64_t)cv.B * cv.H * cv.max_chunks <= kWideDecodeCtas)
+    if ((int64_t)cv.B * cv.H * cv.max_chunks <= kWideCtasPerSm * cv.sms)
       e = launch_split<T, D, 8>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
     else
       e = launch_split<T, D, 4>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
@@ -562,10 +576,10 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
 
 // The cluster path when every head's cache fits one row batch per CTA of a
 // cluster of at most 8 (longer caches are the split-K path's job) and all
-// clusters fit in one wave of the 152 SMs.
+// clusters fit in one wave of the device's SMs (two CTAs per SM).
 bool decode_use_small(const CacheView& cv) {
   const int cl = cluster_size_for(cv);
-  return cl <= kMaxCluster && (int64_t)cv.B * cv.H * cl <= 152 * 2;
+  return cl <= kMaxCluster && (int64_t)cv.B * cv.H * cl <= 2 * (int64_t)cv.sms;
 }
 
 cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,

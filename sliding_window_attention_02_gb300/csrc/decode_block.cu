@@ -15,11 +15,10 @@ namespace rswa {
 // One CTA of NW warps per (b, i, h): the warps split every key segment of
 // query i (prefix, cached outputs of its window, block tokens 0..i) between
 // them, NW * KEYS_WARP rows per round, and merge in shared memory.  8 warps
-// in general; 16 (one CTA per SM) when the grid fits one wave of the 152
-// SMs, so that each query takes half as many dependent row batches.
+// in general; 16 (one CTA per SM) when the grid fits one wave of the
+// device's SMs, so that each query takes half as many dependent row batches.
 constexpr int kBlockWarps = 8;
 constexpr int kBlockWarpsWide = 16;
-constexpr int64_t kBlockWideCtas = 152;
 
 template <typename T, int D, int NW>
 __global__ void __launch_bounds__(NW * 32)
@@ -166,7 +165,7 @@ static cudaError_t launch_block_t(const CacheView& cv, const void* q,
   const int64_t nq = block * cv.H;
   const dim3 grid((unsigned)nq, (unsigned)cv.B);
   cudaError_t e =
-      nq * cv.B <= kBlockWideCtas
+      nq * cv.B <= cv.sms
           ? launch_pdl(decode_block_kernel<T, D, kBlockWarpsWide>, grid,
                        dim3(kBlockWarpsWide * 32), s, cv, (const T*)q, (const T*)k,
                        (const T*)v, block, (T*)o, lse)

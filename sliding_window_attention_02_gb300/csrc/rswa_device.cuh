@@ -63,6 +63,16 @@ __device__ __forceinline__ void cluster_arrive_release() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive without ordering any memory operation (every thread of the CTA
+// executes it together), and a wait that a subset of a warp may execute.
+// A wait returns once every thread of the cluster that has not exited has
+// arrived at the current phase.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_divergent() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
 __device__ __forceinline__ uint32_t map_dsmem(const void* p, uint32_t rank) {
   const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
   uint32_t remote;

@@ -23,7 +23,8 @@ constexpr int kDecodeThreads = 128;     // threads per grouped split-K decode CT
 //                         without cross-head synchronisation; all copies
 //                         of a sequence are equal between calls
 //   err     int32 [1]     first device-side error code (0 = none)
-//   part    float [B][H][max_chunks][d + 2]  split-K partials (m, l, acc)
+//   part    float [B][H][max_chunks][d + 2]  split-K partials (m, l, acc);
+//           the region is sized for the smallest chunk, so it may be larger
 //   cnt_bh  int32 [B][H]  CTAs of (b, h) that have published a partial
 struct CacheView {
   void* K;
@@ -37,6 +38,7 @@ struct CacheView {
   int64_t m_cap, n, slab_rows;
   int chunk;       // keys per decode CTA
   int max_chunks;  // ceil(m_cap / chunk) + ceil(n / chunk)
+  int sms;         // streaming multiprocessors of the cache's device
 };
 
 // Per-launch sequence table for prefill (passed by value as a kernel param).
