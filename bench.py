@@ -6,13 +6,20 @@ the whole hot path over that input: the prefix prefill (cache write +
 attention over the 288 prefix rows) followed by 6000 fused append+decode
 steps through the ring cache.  Value: output tokens/s.
 
-Extra measurements in the same JSON line (the HBM and tensor-core targets):
-  batched_decode   B 64, m_b ~ U{256..2048}, ring full (T 4096), one step
+The JSON line also carries one roofline entry per bound kernel and workload
+(the metric's decode GB/s and prefill TFLOP/s):
   decode_sweep     B 32, m 2600, T in 256 .. 100000: flat per-step latency
+  batched_decode   B 64, m_b ~ U{256..2048}, ring full (T 4096), one step
   prefill          B 1, m 10272, T 22496 (32K rows), 12 independent layers
+  long_prefix      B 1, m 10272 (40 pages), one step through 12 layers
+  batched GQA      B 64, 32 query heads over 8 KV heads
+and the per-step latency of the single-page decode loop at every t, for
+R-SWA and for the standard full cache (n = T).  Everything else measured
+goes to the file named by --extras-out.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
                        [--impl ours|reference] [--no-extras]
+                       [--extras-out PATH]
 """
 
 from __future__ import annotations
@@ -40,6 +47,7 @@ KERNEL_SOURCES = {
     "decode_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh", "tc_ptx.cuh"],
     "decode_cluster_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh",
                               "tc_ptx.cuh"],
+    "decode_gqa_tc_kernel": ["decode_gqa_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
     "prefill_tc_kernel": ["prefill_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
 }
 
@@ -58,9 +66,11 @@ def load_peaks():
 
 
 def kernel_sha(name):
+    """Hash of the sources a kernel is built from ("kernel@workload" keys
+    hash the kernel's)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sliding_window_attention_02_gb300", "csrc")
-    for f in KERNEL_SOURCES[name]:
+    for f in KERNEL_SOURCES.get(name.split("@")[0], []):
         p = os.path.join(csrc, f)
         if os.path.exists(p):
             with open(p, "rb") as fh:
@@ -343,10 +353,11 @@ def run_long_prefix_decode(dev, peaks, layers=12):
                 c.decode_step_fused(steps[0][i][None], steps[1][i][None],
                                     steps[2][i][None], o, stream=s)
         ms = graph_step_ms(step, s, 16, 5)
-        nbytes = layers * H * d * 2 * (2 * (m + n) + 4)
+        per_layer = H * d * 2 * (2 * (m + n) + 4)
+        nbytes = layers * per_layer
         gbs = nbytes / (ms * 1e-3) / 1e9
-        rows.append({"m": m, "us_per_layer": round(ms * 1e3 / layers, 2),
-                     "GB_per_s": round(gbs, 1),
+        rows.append({"m": m, "us_per_layer": round(ms * 1e3 / layers, 3),
+                     "bytes_per_layer": per_layer, "GB_per_s": round(gbs, 1),
                      "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
         del caches
         torch.cuda.empty_cache()
@@ -520,6 +531,91 @@ def graph_step_ms(step, stream, nsteps, iters):
     return statistics.mean(ts) / nsteps
 
 
+def per_step_profile(dev, n=None):
+    """Device time of every decode step of the single-page loop: a CUDA
+    graph of the prefix prefill and the T fused steps with a timing event
+    recorded between consecutive steps (event nodes in the graph).  The
+    event between two steps keeps the next step from starting before the
+    previous one ends, so each figure is the step's whole latency, without
+    the overlap of the back-to-back loop.  Returns per-step microseconds."""
+    import torch
+    import sliding_window_attention_02_gb300 as rswa
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    B, H, d, m, T = w.batch, w.heads, w.head_dim, w.m, w.T
+    n = w.n if n is None else n
+    Q, K, V = workloads.qkv(m + T, H, d, 0, w.std, torch.bfloat16, device=dev)
+    cache = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+    Op = torch.empty(m, H, d, dtype=torch.bfloat16, device=dev)
+    Od = torch.empty(T, B, H, d, dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(T + 1)]
+
+    def body(record):
+        cache.prefill(Q[:m], K[:m], V[:m], Op, [m], 0, stream=s)
+        for t in range(T):
+            if record:
+                ev[t].record(s)
+            cache.decode_step_fused(Q[m + t][None], K[m + t][None],
+                                    V[m + t][None], Od[t], stream=s)
+        if record:
+            ev[T].record(s)
+    with torch.cuda.stream(s):
+        body(False)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        body(True)
+    with torch.cuda.stream(s):
+        g.replay()
+        g.replay()
+    torch.cuda.synchronize(dev)
+    us = [1e3 * ev[t].elapsed_time(ev[t + 1]) for t in range(T)]
+    del g, cache
+    return us
+
+
+def step_stats(us):
+    """p50 / p99 / max / min / mean of a list of per-step microseconds."""
+    xs = sorted(us)
+    q = lambda f: xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))]
+    return {"p50": round(q(0.5), 3), "p99": round(q(0.99), 3),
+            "max": round(xs[-1], 3), "min": round(xs[0], 3),
+            "mean": round(statistics.mean(xs), 3)}
+
+
+def step_growth(us, warm=128):
+    """Least-squares slope (ns per output token) of per-step latency over
+    t >= warm, and the latency ratio of the last 512 steps to steps
+    warm .. warm + 511."""
+    ts = list(range(warm, len(us)))
+    ys = us[warm:]
+    mt, my = statistics.mean(ts), statistics.mean(ys)
+    var = sum((t - mt) ** 2 for t in ts)
+    slope = sum((t - mt) * (y - my) for t, y in zip(ts, ys)) / var
+    ratio = statistics.mean(us[-512:]) / statistics.mean(us[warm:warm + 512])
+    return {"slope_ns_per_token": round(1e3 * slope, 4),
+            "late_to_early": round(ratio, 4)}
+
+
+def boundary_jumps(us, periods=(64, 128, 256), span=8, skip=128):
+    """Latency step at t = multiples of each period (mean of the `span`
+    steps from t minus the mean of the `span` steps before t), against the
+    same statistic at every other t: shows whether per-step latency jumps
+    when the number of cached keys crosses an alignment boundary."""
+    def jump(t):
+        return statistics.mean(us[t:t + span]) - statistics.mean(us[t - span:t])
+    ts = range(max(skip, span), len(us) - span)
+    every = [jump(t) for t in ts]
+    out = {"all_t_mean_us": round(statistics.mean(every), 4),
+           "all_t_p99_us": round(sorted(every)[int(0.99 * (len(every) - 1))], 4)}
+    for p in periods:
+        at = [jump(t) for t in ts if t % p == 0]
+        out[f"at_{p}_mean_us"] = round(statistics.mean(at), 4)
+        out[f"at_{p}_max_us"] = round(max(at), 4)
+    return out
+
+
 def run_extras(dev, peaks, quick=False):
     import torch
     out = {}
@@ -637,9 +733,12 @@ def run_extras(dev, peaks, quick=False):
 # ---------------------------------------------------------------------------
 
 def oracle_single_page_sample(budget_s, max_steps=None):
-    """Oracle time of the single-page workload, extrapolated from a sample:
-    the full 288-row prefix prefill plus the first decode steps until
-    `budget_s` seconds (or max_steps) have elapsed."""
+    """Oracle time of the single-page workload: the 288-row prefix prefill,
+    then the decode steps in order (t = 0, 1, ...) until all T are done or
+    `budget_s` seconds (or max_steps) have passed.  When the budget ends the
+    loop early, the remaining steps are costed at the mean of the steady
+    steps timed (t >= n: every step attends m + n keys, as all later steps
+    do)."""
     import numpy as np
     import torch
     import oracle
@@ -652,18 +751,53 @@ def oracle_single_page_sample(budget_s, max_steps=None):
     oracle.prefill_attention(Q[:m], K[:m], V[:m], m, n)
     state = oracle.prefill_cache(K[:m], V[:m], m, n, 0)
     t1 = time.perf_counter()
-    steps = 0
+    steps, steady, t_steady = 0, 0, 0.0
     while True:
+        a = time.perf_counter()
         state, _, _ = oracle.decode_step_fused(state, Q[m + steps], K[m + steps],
                                                V[m + steps], n)
+        b = time.perf_counter()
+        if steps >= n:
+            steady += 1
+            t_steady += b - a
         steps += 1
-        el = time.perf_counter() - t1
+        el = b - t1
         if el >= budget_s or steps >= T or (max_steps and steps >= max_steps):
             break
-    t_pre, t_dec = t1 - t0, el / steps
-    est = t_pre + T * t_dec
+    t_pre = t1 - t0
+    if steps >= T or steady == 0:
+        est = t_pre + el * T / steps
+    else:
+        est = t_pre + el + (T - steps) * t_steady / steady
     return {"tokens_per_s": T / est, "prefill_s": t_pre, "decode_steps": steps,
-            "decode_s_per_step": t_dec}
+            "decode_s_per_step": el / steps, "whole": steps >= T}
+
+
+def oracle_steady_sampler(n_steps, t_start):
+    """The reference arm's step: `n_steps` fused decode steps of the
+    single-page workload at t = t_start .. t_start + n_steps - 1, after the
+    ring is full (each attends m + n keys per head, as every step past the
+    first n of the workload does).  The cache state at t_start is built once,
+    untimed, by the oracle's own prefill_cache; the oracle's state
+    transitions return new states, so every call starts from it.  Returns a
+    function that runs the sample and returns its seconds."""
+    import torch
+    import oracle
+    import workloads
+    w = workloads.WORKLOADS["single_page_bf16"]
+    H, d, m, n = w.heads, w.head_dim, w.m, w.n
+    Q, K, V = workloads.qkv(m + t_start + n_steps, H, d, 0, w.std, torch.bfloat16)
+    Q, K, V = (x.double().numpy() for x in (Q, K, V))
+    state0 = oracle.prefill_cache(K[:m + t_start], V[:m + t_start], m, n, t_start)
+
+    def run():
+        state = state0
+        t0 = time.perf_counter()
+        for t in range(t_start, t_start + n_steps):
+            state, _, _ = oracle.decode_step_fused(state, Q[m + t], K[m + t],
+                                                   V[m + t], n)
+        return time.perf_counter() - t0
+    return run
 
 
 def host_cores():
@@ -785,32 +919,45 @@ def job_throughput(tokens_per_rank, world_size, ms):
     return tokens_per_rank * world_size / (ms * 1e-3)
 
 
+REF_SAMPLE_STEPS = 500        # decode steps per reference-arm step
+REF_T_START = 5500            # ring full; the workload's last 500 steps
+
+
 def main_reference(args):
+    """The reference arm: the CPU float64 oracle as it stands, on one host
+    thread.  One step of this arm is the sampled region itself - the single
+    page workload's decode steps t = 5500 .. 5999 - so ms_per_step is the
+    time actually spent per step and value is the tokens of that region per
+    second.  (The 288-row prefix prefill and the first n steps, while the
+    ring fills, are about 2 % of the oracle's time on the whole workload and
+    are not in the sample.)"""
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"          # before NumPy loads its BLAS
     import workloads
     w = workloads.WORKLOADS["single_page_bf16"]
+    run = oracle_steady_sampler(REF_SAMPLE_STEPS, REF_T_START)
     for _ in range(args.warmup):
-        run_cpu_worker(0.5, max_steps=100)
-    vals, wall = [], []
-    for _ in range(args.steps):
-        t0 = time.perf_counter()
-        r = run_cpu_worker(0.5, max_steps=100)
-        wall.append(time.perf_counter() - t0)
-        vals.append(r["tokens_per_s"])
-    v = statistics.mean(vals)
-    sample = ("oracle (CPU float64) on the single-page workload: the 288-row "
-              "prefix prefill plus the first 100 decode steps per timed step, "
-              "extrapolated to 6000 steps; one thread")
+        run()
+    secs = [run() for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(secs)
+    v = REF_SAMPLE_STEPS / (ms * 1e-3)
+    sample = ("oracle (CPU float64, one thread) on the single-page workload's "
+              "fused decode steps t = %d..%d (ring full, m + n = %d keys per "
+              "head); one step of this arm = that region"
+              % (REF_T_START, REF_T_START + REF_SAMPLE_STEPS - 1, w.m + w.n))
     line = {
         "impl": "reference", "metric": METRIC, "value": round(v, 2),
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1e3 * w.T / v, 3),
+        "warmup": args.warmup, "ms_per_step": round(ms, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": "single_page_bf16", "batch": 1, "heads": 10,
-                   "head_dim": 128, "m": 288, "n": 128, "T": 6000},
+                   "head_dim": 128, "m": 288, "n": 128, "T": 6000,
+                   "sample": "decode steps t=%d..%d per step"
+                             % (REF_T_START, REF_T_START + REF_SAMPLE_STEPS - 1)},
         "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": sample,
                          "value": round(v, 2), "unit": "tokens/s"},
         "e2e": {"value": round(v, 2), "unit": "tokens/s",
@@ -818,6 +965,63 @@ def main_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def roofline_entry(kernel, workload, bound, work, us, peak, peak_name,
+                   peak_src, traffic_key=None):
+    """One roofline entry: algorithmic bytes (hbm) or flops (tensor) of one
+    launch or step over its device time."""
+    if bound == "hbm":
+        achieved, unit = work / (us * 1e-6) / 1e9, "GB/s"
+    else:
+        achieved, unit = work / (us * 1e-6) / 1e12, "TFLOP/s"
+    return {"kernel": kernel, "workload": workload, "bound": bound,
+            "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4),
+            "traffic": recorded_traffic(traffic_key or kernel),
+            "work": work, "us": round(us, 3), "peak_of": peak_name}
+
+
+def extra_rooflines(extras, peaks, peak_src):
+    """Roofline entries of the bound kernels measured in run_extras."""
+    out = []
+    hbm = peaks["hbm_gbs"]
+    sw = extras.get("decode_sweep")
+    if sw:
+        us = statistics.mean(p["us_per_step"] for p in sw["points"])
+        e = roofline_entry("decode_kernel", "decode_sweep_bf16 (mean over T)",
+                           "hbm", sw["algorithmic_bytes"], us, hbm, "hbm_gbs",
+                           peak_src, "decode_kernel@sweep")
+        e["latency_spread"] = sw["latency_spread"]
+        out.append(e)
+    bt = extras.get("batched_decode")
+    if bt:
+        out.append(roofline_entry("decode_kernel", "batched_decode_bf16", "hbm",
+                                  bt["algorithmic_bytes"], bt["us_per_step"], hbm,
+                                  "hbm_gbs", peak_src, "decode_kernel@batched"))
+    pf = extras.get("prefill")
+    if pf:
+        # 12 back-to-back layers, 13 ms: the burst peak applies
+        out.append(roofline_entry("prefill_tc_kernel", "multipage_prefill_bf16",
+                                  "tensor", pf["algorithmic_flops"],
+                                  1e3 * pf["ms_per_step"], peaks["bf16_tflops"],
+                                  "bf16_tflops", peak_src,
+                                  "prefill_tc_kernel@multipage"))
+    lp = extras.get("long_prefix_decode")
+    if lp:
+        pt = lp["points"][-1]
+        out.append(roofline_entry(lp.get("kernel", "decode_kernel"),
+                                  "long_prefix m=%d (per layer)" % pt["m"], "hbm",
+                                  pt["bytes_per_layer"], pt["us_per_layer"], hbm,
+                                  "hbm_gbs", peak_src,
+                                  lp.get("kernel", "decode_kernel") + "@long_prefix"))
+    gq = extras.get("batched_decode_gqa")
+    if gq:
+        out.append(roofline_entry("decode_gqa_tc_kernel", "batched_decode_gqa",
+                                  "hbm", gq["algorithmic_bytes"], gq["us_per_step"],
+                                  hbm, "hbm_gbs", peak_src,
+                                  "decode_gqa_tc_kernel@batched"))
+    return out
 
 
 def main_ours(args):
@@ -840,7 +1044,8 @@ def main_ours(args):
     ncores = host_cores()
     if rank == 0 and ws == 1 and not args.no_cpu:
         cpu = run_cpu_worker(args.cpu_budget)
-        cpu_all = run_cpu_worker(args.cpu_budget, threads=ncores)
+        if not args.no_extras:
+            cpu_all = run_cpu_worker(args.cpu_budget, threads=ncores)
     cpu_configs = None
     if rank == 0 and ws == 1 and not args.no_cpu and not args.no_extras:
         cpu_configs = run_cpu_configs_worker()
@@ -886,34 +1091,48 @@ def main_ours(args):
     value = job_throughput(w.batch * w.T, ws, ms)
 
     # dominant kernel: fused decode (6000 launches per step)
-    per_launch_ms = statistics.mean(dec_ms) / w.T
-    bpl = single_page_bytes_per_decode(w)
-    achieved = bpl / (per_launch_ms * 1e-3) / 1e9
-    roofline = {"kernel": "decode_cluster_kernel<bf16,128,fused>", "bound": "hbm",
-                "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": recorded_traffic("decode_cluster_kernel"),
-                "peak_source": f"hbm_gbs ({peak_src})",
-                "algorithmic_bytes_per_launch": round(bpl),
-                "launch_us": round(per_launch_ms * 1e3, 3),
-                "note": ("launch duration = decode-graph time / 6000 (includes "
-                         "inter-launch gaps); the 2.1 MB working set stays in "
-                         "L2 across steps, so this batch-1 loop is latency-bound")}
+    per_launch_us = 1e3 * statistics.mean(dec_ms) / w.T
+    head = roofline_entry("decode_cluster_kernel", "single_page_bf16 (headline)",
+                          "hbm", round(single_page_bytes_per_decode(w)),
+                          per_launch_us, peaks["hbm_gbs"], "hbm_gbs", peak_src)
+    head["note"] = ("launch = decode-graph time / 6000; the 2.1 MB cache stays "
+                    "in L2 between steps: latency-bound")
 
     # end-to-end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(sp, dev, args)
+        e2e["eager"] = measure_e2e_eager(sp, dev, args)
+    del sp
+    torch.cuda.empty_cache()
 
-    extras = None
+    extras = {}
+    per_step = None
     if not args.no_extras and rank == 0:
-        del sp
+        try:
+            rs = per_step_profile(dev)
+            mh = per_step_profile(dev, n=w.T)
+            per_step = {"rswa": dict(step_stats(rs), **step_growth(rs)),
+                        "mha": dict(step_stats(mh), **step_growth(mh)),
+                        "mha_jumps": boundary_jumps(mh),
+                        "how": "event between steps in one graph: whole latency "
+                               "of each step, no overlap with its neighbours"}
+            extras["per_step_us"] = {"rswa": [round(x, 3) for x in rs],
+                                     "mha": [round(x, 3) for x in mh]}
+        except Exception as exc:           # events in graphs unsupported
+            per_step = {"unavailable": repr(exc)[:200]}
         torch.cuda.empty_cache()
-        extras = run_extras(dev, peaks, quick=args.quick)
+        extras.update(run_extras(dev, peaks, quick=args.quick))
         if cpu_configs is not None:
             extras["cpu_oracle"] = cpu_configs
+        if cpu_all is not None:
+            extras["cpu_baseline_all_cores"] = {
+                "value": round(cpu_all["tokens_per_s"], 2), "unit": "tokens/s",
+                "cores": ncores, "kind": "oracle"}
+    rooflines = [head] + extra_rooflines(extras, peaks, peak_src)
 
     if rank == 0:
+        sw = extras.get("decode_sweep")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
@@ -926,27 +1145,33 @@ def main_ours(args):
                        "l2": "flushed (256 MB write) before every timed step",
                        "graphs": "prefix prefill and 6000-step decode loop "
                                  "replayed as two CUDA graphs"},
-            "roofline": roofline,
+            "roofline": rooflines,
+            "peaks": {"source": peak_src, "hbm_gbs": peaks["hbm_gbs"],
+                      "bf16_tflops": peaks["bf16_tflops"],
+                      "bf16_tflops_sustained": peaks["bf16_tflops_sustained"]},
+            "per_step_us": per_step,
+            "sweep_us_vs_T": None if not sw else {
+                "T": [p["T"] for p in sw["points"]],
+                "us": [p["us_per_step"] for p in sw["points"]]},
             "cpu_baseline": None if cpu is None else {
                 "value": round(cpu["tokens_per_s"], 2), "unit": "tokens/s",
                 "cores": 1, "kind": "oracle",
-                "sample": ("full 288-row prefix prefill + first %d decode steps "
-                           "(%.1f ms/step) of the same workload, float64, one "
-                           "thread, extrapolated to 6000 steps"
-                           % (cpu["decode_steps"], 1e3 * cpu["decode_s_per_step"]))},
-            "cpu_baseline_all_cores": None if cpu_all is None else {
-                "value": round(cpu_all["tokens_per_s"], 2), "unit": "tokens/s",
-                "cores": ncores, "kind": "oracle",
-                "sample": ("as cpu_baseline, with %d BLAS/OpenMP threads "
-                           "(%d decode steps, %.1f ms/step)"
-                           % (ncores, cpu_all["decode_steps"],
-                              1e3 * cpu_all["decode_s_per_step"]))},
+                "sample": ("the whole workload: 288-row prefix prefill + %d "
+                           "decode steps (%.2f ms/step), float64, one thread"
+                           % (cpu["decode_steps"], 1e3 * cpu["decode_s_per_step"]))
+                          if cpu["whole"] else
+                          ("288-row prefix prefill + the first %d decode steps; "
+                           "the rest costed at the mean steady step; float64, "
+                           "one thread" % cpu["decode_steps"])},
             "e2e": e2e,
             "gpu_launches": args.steps * (2 + w.T),
             "clocks": clocks,
             "cache_bytes_after_T": cache_bytes,
-            "extras": extras,
+            "extras_file": args.extras_out,
         }
+        if args.extras_out:
+            with open(args.extras_out, "w") as f:
+                json.dump(extras, f)
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -956,7 +1181,7 @@ def main_ours(args):
 def measure_e2e(sp, dev, args):
     """Same workload through the public API: per step the inputs are copied
     from pinned host memory and the outputs read back, inside the timed
-    region."""
+    region; the prefill and the 6000 decode calls replay as CUDA graphs."""
     import torch
     w = sp["w"]
     s = sp["stream"]
@@ -990,7 +1215,50 @@ def measure_e2e(sp, dev, args):
     d2h = hOp.numel() * hOp.element_size() + hOd.numel() * hOd.element_size()
     return {"value": round(w.batch * w.T / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms, 4)}
+            "ms_per_step": round(ms, 4), "mode": "graph replay"}
+
+
+def measure_e2e_eager(sp, dev, args, steps=3):
+    """The same end-to-end step with no graph: the host copies, one
+    rswa_prefill call and 6000 rswa_decode_step_fused calls through the C
+    ABI (argument checks, ctypes, launch) per step, timed with events."""
+    import torch
+    w = sp["w"]
+    s = sp["stream"]
+    m, T = w.m, w.T
+    hQ, hK, hV = (x.cpu().pin_memory() for x in (sp["Q"], sp["K"], sp["V"]))
+    hOp = torch.empty_like(sp["Op"], device="cpu").pin_memory()
+    hOd = torch.empty_like(sp["Od"], device="cpu").pin_memory()
+    Q, K, V, Op, Od, cache = (sp[k] for k in ("Q", "K", "V", "Op", "Od", "cache"))
+    q = [Q[m + t][None] for t in range(T)]
+    k = [K[m + t][None] for t in range(T)]
+    v = [V[m + t][None] for t in range(T)]
+
+    def step():
+        with torch.cuda.stream(s):
+            Q.copy_(hQ, non_blocking=True)
+            K.copy_(hK, non_blocking=True)
+            V.copy_(hV, non_blocking=True)
+            cache.prefill(Q[:m], K[:m], V[:m], Op, [m], 0, stream=s)
+            for t in range(T):
+                cache.decode_step_fused(q[t], k[t], v[t], Od[t], stream=s)
+            hOp.copy_(Op, non_blocking=True)
+            hOd.copy_(Od, non_blocking=True)
+    step()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(steps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        step()
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.mean(ts)
+    return {"value": round(w.batch * T / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "us_per_token": round(1e3 * ms / T, 3)}
 
 
 def main_only(args):
@@ -1073,6 +1341,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--quick", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--extras-out", default=None,
+                    help="write every extra measurement to this JSON file")
     ap.add_argument("--cpu-worker", type=float, default=None)
     ap.add_argument("--cpu-configs-worker", action="store_true")
     ap.add_argument("--cpu-max-steps", type=int, default=None)
