@@ -83,7 +83,7 @@ int run_decode(rswa_cache* cache, F launch) {
 struct Layout {
   size_t m_off, t_off, err_off, k_off, v_off, part_off, cnt_bh_off;
   size_t total;
-  int chunk, max_chunks;
+  int chunk, max_chunks, part_slots;
 };
 
 int valid_shape(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
@@ -160,6 +160,7 @@ Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
   L.max_chunks = (int)((m + L.chunk - 1) / L.chunk + (n + L.chunk - 1) / L.chunk);
   const int64_t chunks_bound = (m + kMinChunk - 1) / kMinChunk +
                                (n + kMinChunk - 1) / kMinChunk;
+  L.part_slots = (int)std::min<int64_t>(chunks_bound, INT32_MAX);
   size_t off = 0;
   L.m_off = off;      off = align_up(off + sizeof(int32_t) * batch);
   L.t_off = off;      off = align_up(off + sizeof(int64_t) * batch * heads);
@@ -261,6 +262,7 @@ int rswa_cache_create_gqa(int64_t m, int64_t n, int heads, int kv_heads,
   cv.chunk = L.chunk;
   cv.max_chunks = L.max_chunks;
   cv.sms = sms;
+  cv.part_slots = L.part_slots;
   c->device = dev;
   c->buf = device_buf;
   c->buf_bytes = buf_bytes;

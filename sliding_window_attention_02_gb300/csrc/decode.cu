@@ -10,6 +10,8 @@
 // arrive (atomic counter, no waiting) merges the partials and writes o and
 // lse.  Per-step cost is m_b + min(n, t_b) keys: flat in t_b once t_b >= n
 // ("Unlimited OCR", GeekNews, kernel analysis).
+#include <algorithm>
+
 #include "attend.cuh"
 #include "tc_ptx.cuh"
 
@@ -175,6 +177,12 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     }
   }
 }
+
+// 1: few heads with long caches stream through shared memory
+// (decode_stream.cu); 0: they take the split-K kernel.
+#ifndef RSWA_STREAM_DECODE
+#define RSWA_STREAM_DECODE 1
+#endif
 
 constexpr uint32_t kMaxClusterSize = 8;
 // Loads in flight per lane in the cluster path: 4 measured best on GB300 for
@@ -556,6 +564,8 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
     else
       e = launch_cluster<T, D, false>(cv, qq, nullptr, nullptr, oo, lse,
                                       prefetch, s);
+  } else if (RSWA_STREAM_DECODE && decode_use_stream(cv)) {
+    return launch_decode_stream(cv, q, k, v, o, lse, fused, prefetch, s);
   } else if constexpr (sizeof(T) == 2) {
     if ((int64_t)cv.B * cv.H * cv.max_chunks <= kWideCtasPerSm * cv.sms)
       e = launch_split<T, D, 8>(cv, qq, kk, vv, oo, lse, fused, prefetch, s);
@@ -600,6 +610,15 @@ cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
   if (cv.d == 64)
     return launch_decode_t<__nv_bfloat16, 64>(cv, q, k, v, o, lse, fused, pf, s);
   return launch_decode_t<__nv_bfloat16, 128>(cv, q, k, v, o, lse, fused, pf, s);
+}
+
+// Partial slots per (b, h) of the decode path launch_decode takes for cv.
+int decode_part_slots(const CacheView& cv) {
+  if (!decode_use_small(cv) && RSWA_STREAM_DECODE && decode_use_stream(cv) &&
+      !(cv.H != cv.Hkv && ((RSWA_GQA_TC && gqa_tc_supported(cv)) ||
+                           decode_gqa_heads_per_cta(cv) > 1)))
+    return std::max(cv.max_chunks, decode_stream_splits(cv));
+  return cv.max_chunks;
 }
 
 }  // namespace rswa

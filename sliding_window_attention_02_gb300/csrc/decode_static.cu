@@ -45,8 +45,8 @@ namespace rswa {
 // Bytes of static scratch a cache view needs: partials, then counters.
 size_t static_scratch_need(const CacheView& cv, size_t* part_bytes,
                            size_t* cnt_bytes) {
-  *part_bytes = align256(sizeof(float) * (size_t)cv.B * cv.H * cv.max_chunks *
-                         (cv.d + 2));
+  *part_bytes = align256(sizeof(float) * (size_t)cv.B * cv.H *
+                         decode_part_slots(cv) * (cv.d + 2));
   *cnt_bytes = align256(sizeof(int32_t) * (size_t)cv.B * cv.H);
   return *part_bytes + *cnt_bytes;
 }
@@ -68,6 +68,7 @@ cudaError_t launch_decode_fused_static(const CacheView& cv, int dev,
   char* b = static_cast<char*>(base);
   CacheView sv = cv;
   sv.part = reinterpret_cast<float*>(b);
+  sv.part_slots = decode_part_slots(cv);
   sv.cnt_bh = reinterpret_cast<int32_t*>(b + part_bytes);
   e = cudaMemsetAsync(sv.cnt_bh, 0, cnt_bytes, s);
   if (e != cudaSuccess) return e;

@@ -39,6 +39,7 @@ struct CacheView {
   int chunk;       // keys per decode CTA
   int max_chunks;  // ceil(m_cap / chunk) + ceil(n / chunk)
   int sms;         // streaming multiprocessors of the cache's device
+  int part_slots;  // partial slots per (b, h) in `part` (>= max_chunks)
 };
 
 // Per-launch sequence table for prefill (passed by value as a kernel param).
@@ -60,6 +61,16 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
 cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
                          cudaStream_t s);
 bool decode_use_small(const CacheView& cv);
+// Few heads with long caches (decode_stream.cu): S CTAs per head stream the
+// head's keys through shared memory; S <= part_slots.
+bool decode_use_stream(const CacheView& cv);
+int decode_stream_splits(const CacheView& cv);
+cudaError_t launch_decode_stream(const CacheView& cv, const void* q,
+                                 const void* k, const void* v, void* o,
+                                 float* lse, bool fused, bool prefetch_prefix,
+                                 cudaStream_t s);
+// Partial slots per (b, h) the decode path chosen for this view uses.
+int decode_part_slots(const CacheView& cv);
 // Grouped split-K decode (decode_gqa.cu): used for grouped caches whose query
 // heads per KV head are a multiple of 2 when the cluster path is not taken.
 // Query heads one CTA serves (4, 2, or 1 = not grouped); the chunk heuristic

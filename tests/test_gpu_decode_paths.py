@@ -1,0 +1,190 @@
+"""GPU parity of the decode paths chosen by shape, against the CPU float64
+oracle through the C ABI.
+
+* Few heads with long caches: the shared-memory streaming kernel
+  (decode_stream.cu), S CTAs per head over [prefix | ring].  Ragged prefixes,
+  an empty prefix, a ring that wraps, float32 and head_dim 64, grouped heads
+  that no grouped kernel takes, fused and unfused steps enqueued back to
+  back (the launches after the first read prefix rows before their
+  dependency wait), and the 40-page single-sequence shape.
+* Grouped heads on the tensor cores, several fused steps back to back at a
+  batched shape whose grid takes more than one wave of CTAs.
+
+Tolerances as in test_gpu_parity: float32 max |err| <= 1e-4; bf16 max |err|
+<= 2e-2 and mean |err| <= 5e-3; t_b and cache sizes bit-exact.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+BF16_MAX, BF16_MEAN = 2e-2, 5e-3
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def assert_close(got, ref, dtype, what=""):
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    assert np.isfinite(err).all(), what
+    if dtype == 0:
+        assert err.max() <= F32_TOL, f"{what}: max {err.max():.3e}"
+    else:
+        assert err.max() <= BF16_MAX, f"{what}: max {err.max():.3e}"
+        assert err.mean() <= BF16_MEAN, f"{what}: mean {err.mean():.3e}"
+
+
+def tdt(dtype):
+    return torch.float32 if dtype == 0 else torch.bfloat16
+
+
+# Each case moves at least 96 KB of keys and values per SM of a 152-SM GB300
+# (the streaming kernel's threshold); the last two are below it and check
+# the split-K fallback of the same shapes.
+STREAM_CASES = [
+    # (m_list, n, H, Hkv, d, dtype, steps, t0)  t0: restored t_b (None: 0)
+    ([3000, 1200, 0], 64, 4, 4, 128, 1, 150, None),
+    ([9000], 128, 4, 4, 64, 0, 40, None),
+    ([4000], 64, 4, 4, 128, 0, 70, None),
+    ([14000], 256, 5, 5, 64, 1, 20, 4096 + 37),
+    ([1700, 640], 16, 6, 2, 128, 0, 35, None),   # 3 query heads per KV head
+    ([10272], 128, 10, 10, 128, 1, 3, 4096 + 37),  # one sequence, 40 pages
+    ([2000], 128, 3, 3, 64, 0, 40, None),
+    ([900], 32, 2, 2, 128, 0, 70, None),
+]
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("case", STREAM_CASES,
+                         ids=lambda c: f"m{c[0]}n{c[1]}H{c[2]}kv{c[3]}d{c[4]}dt{c[5]}")
+def test_stream_decode(cuda_lib, case, fused):
+    rswa = cuda_lib
+    m_list, n, H, Hkv, d, dtype, steps, t0 = case
+    B = len(m_list)
+    dt = tdt(dtype)
+    T = n if t0 is not None else 0           # outputs prefilled into the ring
+    rows = [m + T for m in m_list]
+    K = workloads.normal((sum(rows), Hkv, d), 301, 1.0, dt)
+    V = workloads.normal((sum(rows), Hkv, d), 302, 1.0, dt)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, dtype, kv_heads=Hkv)
+    cache.prefill(None, K.cuda(), V.cuda(), None, m_list, T)
+    offs = np.cumsum([0] + rows)
+    states = [oracle.prefill_cache(f64(K[offs[b]:offs[b + 1]]),
+                                   f64(V[offs[b]:offs[b + 1]]), m_list[b], n, T)
+              for b in range(B)]
+    if t0 is not None:
+        cache.set_t([t0] * B)
+        for st in states:
+            st["t"] = t0                     # same ring contents, restored t_b
+    q_all = workloads.normal((steps * B, H, d), 303, 1.0, dt).cuda()
+    k_all = workloads.normal((steps * B, Hkv, d), 304, 1.0, dt).cuda()
+    v_all = workloads.normal((steps * B, Hkv, d), 305, 1.0, dt).cuda()
+    o = torch.empty(steps, B, H, d, dtype=dt, device="cuda")
+    lse = torch.empty(steps, B, H, device="cuda")
+    for s in range(steps):                   # enqueued back to back
+        q, k, v = (x[s * B:(s + 1) * B] for x in (q_all, k_all, v_all))
+        if fused:
+            cache.decode_step_fused(q, k, v, o[s], lse[s])
+        else:
+            cache.append_kv(k, v)
+            cache.decode_step(q, o[s], lse[s])
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for s in range(steps):
+        for b in range(B):
+            sl = s * B + b
+            states[b], ro, rl = oracle.decode_step_fused(
+                states[b], f64(q_all[sl]), f64(k_all[sl]), f64(v_all[sl]), n)
+            assert_close(f64(o[s, b]), ro, dtype, f"step {s} seq {b}")
+            assert np.abs(f64(lse[s, b]) - rl).max() <= (1e-4 if dtype == 0 else 1e-3)
+    t_end = (t0 or 0) + steps
+    for b, m in enumerate(m_list):
+        assert cache.get_t(b) == t_end
+        assert cache.cache_len(b) == oracle.cache_len(m, n, t_end)
+    # the ring holds exactly the oracle's slots
+    Ks, Vs = cache.slabs()
+    m_cap = max(m_list)
+    for b in range(B):
+        held = sorted(oracle.ring_outputs(t_end, n))
+        np.testing.assert_array_equal(
+            f64(Ks[b, :, m_cap:])[:, held].transpose(1, 0, 2), states[b]["Kr"][held])
+        np.testing.assert_array_equal(
+            f64(Vs[b, :, m_cap:])[:, held].transpose(1, 0, 2), states[b]["Vr"][held])
+
+
+def test_stream_decode_after_reprefill(cuda_lib):
+    """The first decode launch after a prefill may not read the prefix before
+    its dependency wait; later ones may.  Prefill prefix A, decode, prefill a
+    different prefix B into the same long cache and decode at once, all
+    back to back on one stream."""
+    rswa = cuda_lib
+    m, n, H, d, steps = 4128, 128, 8, 128, 3      # 17 MB: the streaming kernel
+    cache = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16)
+    outs, refs = [], []
+    for seed in (41, 42):
+        K = workloads.normal((m, H, d), seed, 1.0, torch.bfloat16)
+        V = workloads.normal((m, H, d), seed + 100, 1.0, torch.bfloat16)
+        q = workloads.normal((steps, H, d), seed + 200, 1.0, torch.bfloat16)
+        k = workloads.normal((steps, H, d), seed + 300, 1.0, torch.bfloat16)
+        v = workloads.normal((steps, H, d), seed + 400, 1.0, torch.bfloat16)
+        cache.prefill(None, K.cuda(), V.cuda(), None, [m], 0)
+        o = torch.empty(steps, 1, H, d, dtype=torch.bfloat16, device="cuda")
+        for s in range(steps):
+            cache.decode_step_fused(q[s][None].cuda(), k[s][None].cuda(),
+                                    v[s][None].cuda(), o[s])
+        outs.append(o)
+        st = oracle.prefill_cache(f64(K), f64(V), m, n, 0)
+        r = []
+        for s in range(steps):
+            st, ro, _ = oracle.decode_step_fused(st, f64(q[s]), f64(k[s]), f64(v[s]), n)
+            r.append(ro)
+        refs.append(np.stack(r))
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for o, r in zip(outs, refs):
+        assert_close(f64(o[:, 0]), r, 1, "after prefill")
+
+
+def test_gqa_tc_back_to_back(cuda_lib):
+    """Several fused grouped-head steps on the tensor cores enqueued back to
+    back at a batched shape (more CTAs than one wave, two per SM sharing its
+    TMEM): each step's next-launch trigger fires right after its dependency
+    wait.  Every step is checked against the oracle."""
+    rswa = cuda_lib
+    B, H, Hkv, d, n, steps = 48, 16, 4, 128, 128, 4
+    m_list = workloads.prefix_lengths(B, 200, 1400, seed=11)
+    T = 130                                  # the ring has wrapped once
+    rows = [m + T for m in m_list]
+    K = workloads.normal((sum(rows), Hkv, d), 311, 1.0, torch.bfloat16)
+    V = workloads.normal((sum(rows), Hkv, d), 312, 1.0, torch.bfloat16)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    cache.prefill(None, K.cuda(), V.cuda(), None, m_list, T)
+    offs = np.cumsum([0] + rows)
+    states = [oracle.prefill_cache(f64(K[offs[b]:offs[b + 1]]),
+                                   f64(V[offs[b]:offs[b + 1]]), m_list[b], n, T)
+              for b in range(B)]
+    q_all = workloads.normal((steps * B, H, d), 313, 1.0, torch.bfloat16).cuda()
+    k_all = workloads.normal((steps * B, Hkv, d), 314, 1.0, torch.bfloat16).cuda()
+    v_all = workloads.normal((steps * B, Hkv, d), 315, 1.0, torch.bfloat16).cuda()
+    o = torch.empty(steps, B, H, d, dtype=torch.bfloat16, device="cuda")
+    for s in range(steps):
+        cache.decode_step_fused(*(x[s * B:(s + 1) * B] for x in (q_all, k_all, v_all)),
+                                o[s])
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for s in range(steps):
+        got = f64(o[s])
+        for b in range(B):
+            sl = s * B + b
+            states[b], ro, _ = oracle.decode_step_fused(
+                states[b], f64(q_all[sl]), f64(k_all[sl]), f64(v_all[sl]), n)
+            assert_close(got[b], ro, 1, f"step {s} seq {b}")
+    for b in range(B):
+        assert cache.get_t(b) == T + steps
