@@ -48,6 +48,8 @@ KERNEL_SOURCES = {
     "decode_cluster_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh",
                               "tc_ptx.cuh"],
     "decode_gqa_tc_kernel": ["decode_gqa_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
+    "decode_stream_kernel": ["decode_stream.cu", "attend.cuh", "rswa_device.cuh",
+                             "tc_ptx.cuh"],
     "prefill_tc_kernel": ["prefill_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
 }
 
@@ -361,7 +363,8 @@ def run_long_prefix_decode(dev, peaks, layers=12):
                      "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)})
         del caches
         torch.cuda.empty_cache()
-    return {"workload": "B1 H10 d128 n128 bf16 fused decode through %d layers' "
+    return {"kernel": "decode_stream_kernel",
+            "workload": "B1 H10 d128 n128 bf16 fused decode through %d layers' "
                         "caches, prefix of 4/16/40 pages (%.2f GB per step at "
                         "40 pages, from HBM)" % (
                             layers, layers * 10 * 128 * 2 * 2 * (10272 + 128) / 1e9),

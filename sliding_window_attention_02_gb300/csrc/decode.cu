@@ -156,13 +156,11 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     P[c * (D + 2)] = M;
     P[c * (D + 2) + 1] = Ls;
   }
-  __threadfence();
   __syncthreads();
   __shared__ int s_last;
-  if (tid == 0) s_last = (atomicAdd(&cv.cnt_bh[bh], 1) == nch - 1);
+  if (tid == 0) s_last = arrive_acq_rel(&cv.cnt_bh[bh]) == nch - 1;
   __syncthreads();
   if (s_last) {
-    __threadfence();
     float r2, Lt, At;
     // Up to 16 chunks per round trip: a batch-1 head with a 40-page prefix
     // has 42 chunks, and this merge is the last step of the decode.

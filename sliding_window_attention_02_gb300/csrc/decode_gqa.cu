@@ -134,13 +134,11 @@ __device__ __forceinline__ void gqa_combine(const CacheView& cv,
       P[1] = Ls;
     }
   }
-  __threadfence();
   __syncthreads();
   __shared__ int s_last;
-  if (tid == 0) s_last = (atomicAdd(&cv.cnt_bh[ck.bh0], 1) == ck.nch - 1);
+  if (tid == 0) s_last = arrive_acq_rel(&cv.cnt_bh[ck.bh0]) == ck.nch - 1;
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   float M[G], L[G], A[G];
   merge_partials<G, 1>(
       cv.part + ck.bh0 * cv.max_chunks * (D + 2), (size_t)cv.max_chunks * (D + 2),

@@ -89,10 +89,14 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
 // PREFETCH: the preceding kernel of the stream writes no prefix row, so a
 // prefix slot's first K and V tiles may be requested before the dependency
 // wait.
+// tmK8 / tmV8: the same slabs with 8-row boxes, for the rows of a chunk's
+// last tile (whole 8-row groups; the tile's other rows are not fetched).
 template <bool FUSED, int G, bool PREFETCH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, CacheView cv,
+                     const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmK8,
+                     const __grid_constant__ CUtensorMap tmV8, CacheView cv,
                      const __nv_bfloat16* __restrict__ q,
                      const __nv_bfloat16* __restrict__ knew,
                      const __nv_bfloat16* __restrict__ vnew,
@@ -125,6 +129,13 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     tmem_alloc(smem_u32(tmem_slot), TM_COLS);
     tmem_relinquish();
   }
+  // Zero the ring slots: a chunk's last tile fetches only its rows (in
+  // 8-row groups), and the rows it leaves keep what the slot held before -
+  // zeros, or rows of an earlier tile - finite values that the masked
+  // probabilities (p = 0) multiply exactly to 0.
+  for (uint32_t i = tid; i < NS * kTileB / 16; i += kThreads)
+    reinterpret_cast<uint4*>(smem + OFF_RING)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
   __syncthreads();                                  // barriers initialised
   // A prefix slot's first K and V tiles start at slab row y * chunk whatever
   // m_b is: request them (ring slots 0 and 1, loads 0 and 1 of the chunk)
@@ -196,15 +207,30 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   }
   const int nt = (int)((j1 - j0 + BN - 1) / BN);   // tiles of this chunk
   const int64_t rbase = (int64_t)bkv * cv.slab_rows + j0;
-  // K_i (even idx) or V_i (odd idx) into ring slot idx % NS.
+  // Rows of the last tile, rounded up to whole 8-row groups.
+  const int last8 = nt > 0 ? (int)((j1 - j0 - (int64_t)(nt - 1) * BN + 7) & ~7) : BN;
+  // K_i (even idx) or V_i (odd idx) into ring slot idx % NS; the last tile
+  // as 8-row boxes, each landing at its rows' place in the swizzled tile
+  // (1 KB-aligned, so the 128-byte swizzle pattern is the full tile's).
   auto load = [&](int idx) {
     const int s = idx % NS;
-    const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
+    const bool isv = idx & 1;
     const int y = (int)(rbase + (int64_t)(idx >> 1) * BN);
     const uint32_t dst = sb + OFF_RING + s * kTileB;
-    mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
-    tma_load_2d(dst, map, 0, y, bar(B_FULL + s));
-    tma_load_2d(dst + kSub, map, 64, y, bar(B_FULL + s));
+    const int rows = (idx >> 1) == nt - 1 ? last8 : BN;
+    if (rows == BN) {
+      const CUtensorMap* map = isv ? &tmV : &tmK;
+      mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
+      tma_load_2d(dst, map, 0, y, bar(B_FULL + s));
+      tma_load_2d(dst + kSub, map, 64, y, bar(B_FULL + s));
+    } else {
+      const CUtensorMap* map = isv ? &tmV8 : &tmK8;
+      mbar_arrive_expect_tx(bar(B_FULL + s), (uint32_t)rows * 256u);
+      for (int r = 0; r < rows; r += 8) {
+        tma_load_2d(dst + r * 128, map, 0, y + r, bar(B_FULL + s));
+        tma_load_2d(dst + kSub + r * 128, map, 64, y + r, bar(B_FULL + s));
+      }
+    }
   };
   const int first_loads = min(NS, 2 * nt);
 
@@ -452,12 +478,10 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       }
     }
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) *s_last = live && (atomicAdd(&cv.cnt_bh[bh0], 1) == nch - 1);
+  if (tid == 0) *s_last = live && arrive_acq_rel(&cv.cnt_bh[bh0]) == nch - 1;
   __syncthreads();
   if (*s_last && tid < kSoftThreads) {
-    __threadfence();
     float M[G], L[G], A[G];
     merge_partials<G, (G <= 2 ? 2 : 1)>(
         cv.part + bh0 * cv.max_chunks * (HD + 2), (size_t)cv.max_chunks * (HD + 2),
@@ -490,7 +514,8 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
 
 template <bool FUSED, int G, bool PREFETCH>
 cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
-                      const CUtensorMap& mv, const void* q, const void* k,
+                      const CUtensorMap& mv, const CUtensorMap& mk8,
+                      const CUtensorMap& mv8, const void* q, const void* k,
                       const void* v, void* o, float* lse, cudaStream_t s) {
   auto kern = decode_gqa_tc_kernel<FUSED, G, PREFETCH>;
   // Per device (the attribute belongs to the current device's context).
@@ -508,20 +533,23 @@ cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   using BF = __nv_bfloat16;
-  return cudaLaunchKernelEx(&cfg, kern, mk, mv, cv, (const BF*)q,
+  return cudaLaunchKernelEx(&cfg, kern, mk, mv, mk8, mv8, cv, (const BF*)q,
                             (const BF*)(FUSED ? k : nullptr),
                             (const BF*)(FUSED ? v : nullptr), (BF*)o, lse);
 }
 
 template <bool FUSED, bool PREFETCH>
-cudaError_t launch_tc_g(const CacheView& cv, const CUtensorMap& mk,
-                        const CUtensorMap& mv, const void* q, const void* k,
-                        const void* v, void* o, float* lse, cudaStream_t s) {
+cudaError_t launch_tc_g(const CacheView& cv, const CUtensorMap* m, const void* q,
+                        const void* k, const void* v, void* o, float* lse,
+                        cudaStream_t s) {
   const int per_kv = cv.H / cv.Hkv;
-  if (per_kv <= 2) return launch_tc<FUSED, 2, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
-  if (per_kv <= 4) return launch_tc<FUSED, 4, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
-  if (per_kv <= 8) return launch_tc<FUSED, 8, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
-  return launch_tc<FUSED, 16, PREFETCH>(cv, mk, mv, q, k, v, o, lse, s);
+  if (per_kv <= 2)
+    return launch_tc<FUSED, 2, PREFETCH>(cv, m[0], m[1], m[2], m[3], q, k, v, o, lse, s);
+  if (per_kv <= 4)
+    return launch_tc<FUSED, 4, PREFETCH>(cv, m[0], m[1], m[2], m[3], q, k, v, o, lse, s);
+  if (per_kv <= 8)
+    return launch_tc<FUSED, 8, PREFETCH>(cv, m[0], m[1], m[2], m[3], q, k, v, o, lse, s);
+  return launch_tc<FUSED, 16, PREFETCH>(cv, m[0], m[1], m[2], m[3], q, k, v, o, lse, s);
 }
 
 }  // namespace
@@ -538,17 +566,19 @@ cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,
                                  float* lse, bool fused, bool prefetch_prefix,
                                  cudaStream_t s) {
   const uint64_t rows = (uint64_t)cv.B * cv.Hkv * cv.slab_rows;
-  CUtensorMap mk, mv;
-  if (!make_tmap_rows_bf16(&mk, cv.K, HD, rows) ||
-      !make_tmap_rows_bf16(&mv, cv.V, HD, rows))
+  CUtensorMap m[4];                                 // K, V; K, V in 8-row boxes
+  if (!make_tmap_rows_bf16(&m[0], cv.K, HD, rows) ||
+      !make_tmap_rows_bf16(&m[1], cv.V, HD, rows) ||
+      !make_tmap_rows_bf16(&m[2], cv.K, HD, rows, 8) ||
+      !make_tmap_rows_bf16(&m[3], cv.V, HD, rows, 8))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (prefetch_prefix)
-    e = fused ? launch_tc_g<true, true>(cv, mk, mv, q, k, v, o, lse, s)
-              : launch_tc_g<false, true>(cv, mk, mv, q, k, v, o, lse, s);
+    e = fused ? launch_tc_g<true, true>(cv, m, q, k, v, o, lse, s)
+              : launch_tc_g<false, true>(cv, m, q, k, v, o, lse, s);
   else
-    e = fused ? launch_tc_g<true, false>(cv, mk, mv, q, k, v, o, lse, s)
-              : launch_tc_g<false, false>(cv, mk, mv, q, k, v, o, lse, s);
+    e = fused ? launch_tc_g<true, false>(cv, m, q, k, v, o, lse, s)
+              : launch_tc_g<false, false>(cv, m, q, k, v, o, lse, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -51,6 +51,13 @@ constexpr int kWarps = RSWA_STREAM_WARPS;        // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kU = 4;                            // rows per lane group and stage
 constexpr int NS = RSWA_STREAM_STAGES;           // stages
+// Stages a CTA may request before its dependency wait: 2 measured best on
+// GB300 for the 40-page step (13.3 against 13.7 us per layer with all 6);
+// more early traffic slows the previous launch's combine.
+#ifndef RSWA_STREAM_EARLY_STAGES
+#define RSWA_STREAM_EARLY_STAGES 2
+#endif
+constexpr int kEarlyStages = RSWA_STREAM_EARLY_STAGES;
 constexpr uint32_t kTensorStage = kWarps * kU * 512;   // K (or V) bytes of a stage
 constexpr uint32_t kStageBytes = 2 * kTensorStage;
 constexpr uint32_t OFF_BAR = NS * kStageBytes;
@@ -149,7 +156,7 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     if (producer && lane == 0) {
       // Stages made only of prefix rows: their addresses and contents are
       // fixed until the next prefill.
-      while (issued < min(nst, NS) &&
+      while (issued < min(nst, kEarlyStages) &&
              min(span0 + (int64_t)(issued + 1) * SR, span1) <= m_b) {
         issue(issued);
         ++issued;
@@ -271,12 +278,10 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     P[c * (D + 2)] = M;
     P[c * (D + 2) + 1] = Ls;
   }
-  __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&cv.cnt_bh[bh], 1) == nch - 1);
+  if (tid == 0) s_last = arrive_acq_rel(&cv.cnt_bh[bh]) == nch - 1;
   __syncthreads();
   if (s_last) {
-    __threadfence();
     float r2, Lt, At;
     merge_partials<1, 16>(P, 0, nch, D, tid, 1, &r2, &Lt, &At);
     if (tid < D) o[bh * D + tid] = (T)(Lt > 0.f ? At / Lt : 0.f);
@@ -335,9 +340,13 @@ int stage_rows(const CacheView& cv) {
 // CTAs per head: one CTA per SM over all (b, h), at most one per stage of
 // the head's m_cap + n rows, and no more than the partial slots the cache
 // reserves per head.
+#ifndef RSWA_STREAM_MAX_SPLITS
+#define RSWA_STREAM_MAX_SPLITS 1024
+#endif
+
 int decode_stream_splits(const CacheView& cv) {
   const int64_t heads = (int64_t)cv.B * cv.H;
-  int64_t S = cv.sms / heads;
+  int64_t S = std::min<int64_t>(cv.sms / heads, RSWA_STREAM_MAX_SPLITS);
   const int64_t sr = stage_rows(cv);
   S = std::min<int64_t>(S, (cv.m_cap + cv.n + sr - 1) / sr);
   S = std::min<int64_t>(S, cv.part_slots);

@@ -715,12 +715,12 @@ bool make_map(CUtensorMap* map, const void* base, int H, int64_t rows) {
 }  // namespace
 
 bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
-                         uint64_t rows) {
+                         uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

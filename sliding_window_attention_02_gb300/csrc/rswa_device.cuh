@@ -128,6 +128,22 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Arrival on a split-K counter: atomically adds 1 with release and acquire
+// semantics at GPU scope and returns the old value.  Issued by one thread
+// after a CTA barrier, the release orders every store the CTA made before
+// the barrier (the CTA's partial) before the increment; the acquire orders
+// the increment before the loads that follow, so the last CTA to arrive
+// sees every other CTA's partial.  Replaces a fence, a relaxed add and a
+// second fence.
+__device__ __forceinline__ int arrive_acq_rel(int32_t* counter) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;"
+               : "=r"(old)
+               : "l"(counter)
+               : "memory");
+  return old;
+}
+
 // 16-byte streaming load through the read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;

@@ -95,10 +95,10 @@ cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,
                                  const void* k, const void* v, void* o,
                                  float* lse, bool fused, bool prefetch_prefix,
                                  cudaStream_t s);
-// [rows][cols] bf16, row-major, as a 2-D TMA map: box 64 columns x 128 rows,
-// 128-byte swizzle; rows past `rows` read as zero.
+// [rows][cols] bf16, row-major, as a 2-D TMA map: box 64 columns x box_rows
+// rows, 128-byte swizzle; rows past `rows` read as zero.
 bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
-                         uint64_t rows);
+                         uint64_t rows, uint32_t box_rows = 128);
 cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
                               const void* v, void* o, float* lse, bool fused,
                               cudaStream_t s);
