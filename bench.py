@@ -371,10 +371,11 @@ def run_long_prefix_decode(dev, peaks, layers=12):
             "points": rows}
 
 
-def run_block_decode(dev, peaks, blocks=(1, 4, 16, 64), reps=16):
+def run_block_decode(dev, peaks, blocks=(1, 4, 16, 64, 256, 1024), reps=16):
     """Multi-query decode (rswa_decode_block) on the single-page cache: one
     call decodes and appends `block` consecutive tokens per sequence (the
-    shape of verifying drafted tokens).  Per call latency and tokens/s."""
+    shape of verifying drafted tokens; past n = 128, chunked prefill of
+    output text into the cache).  Per call latency and tokens/s."""
     import torch
     import sliding_window_attention_02_gb300 as rswa
     import workloads
@@ -401,7 +402,8 @@ def run_block_decode(dev, peaks, blocks=(1, 4, 16, 64), reps=16):
                      "tokens_per_s": round(B * k / (ms * 1e-3), 1)})
         del c, Q, K, V
     return {"workload": "B1 H10 d128 m288 n128 bf16 (single-page cache), "
-                        "rswa_decode_block with blocks of 1/4/16/64 tokens",
+                        "rswa_decode_block with blocks of %s tokens"
+                        % "/".join(str(b) for b in blocks),
             "points": rows}
 
 

@@ -204,22 +204,25 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
 
 /*
  * Decode a block of `block` consecutive output tokens per sequence in one
- * call (1 <= block <= n): q, o are [B][block][H][d] and k, v are
+ * call (1 <= block <= 2^24): q, o are [B][block][H][d] and k, v are
  * [B][block][H_kv][d] for outputs t_b .. t_b + block - 1; lse (may be NULL)
  * is [B][block][H] float32.
  * Output t_b + i attends to the prefix, to the cached outputs of its window
- * j in [max(0, t_b + i - n + 1), t_b), and to block tokens 0..i - exactly
- * what `block` single steps would give (N(t) = P U D_n(t), "Unlimited-OCR
- * deep dive" pseudo-code block).  The block's keys and values are then
- * appended (slots (t_b + i) mod n) and t_b advances by `block`.  For
- * verifying drafted tokens or prefilling output text into an existing cache.
+ * j in [max(0, t_b + i - n + 1), t_b), and to the block's tokens of its
+ * window, i' in [max(0, i - n + 1), i] - exactly what `block` single steps
+ * would give (N(t) = P U D_n(t), "Unlimited-OCR deep dive" pseudo-code
+ * block).  Afterwards the ring holds the last n outputs (slot j mod n; a
+ * block longer than n replaces the whole ring with its last n tokens) and
+ * t_b has advanced by `block`.  For verifying drafted tokens (a few tokens)
+ * or prefilling output text into an existing cache (any length).
  * block == 1 runs rswa_decode_step_fused (same layouts), so the prefix
  * ordering rule of rswa_decode_step holds for every block size.  Larger
- * blocks take two kernels on `stream`: attention, then the append, which
- * waits for the attention kernel to finish (the ring slots it overwrites
- * are read by the block's earlier outputs).
- * Errors: RSWA_EINVAL (block outside 1..n, null or misaligned pointers),
- * RSWA_EHANDLE, RSWA_ECUDA.
+ * blocks take two kernels on `stream`: attention (on the tensor cores for
+ * bf16, head_dim 128 and blocks of 16 or more; else on the CUDA cores), then
+ * the append, which waits for the attention kernel to finish (the ring
+ * slots it overwrites are read by the block's earlier outputs).
+ * Errors: RSWA_EINVAL (block outside 1..2^24, batch above 65535, null or
+ * misaligned pointers), RSWA_EHANDLE, RSWA_ECUDA.
  */
 RSWA_API int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
                                const void* v, int64_t block, void* o,

@@ -402,7 +402,11 @@ int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
                       const void* v, int64_t block, void* o, float* lse,
                       void* stream) {
   if (!live(cache)) return RSWA_EHANDLE;
-  if (block < 1 || block > cache->cv.n) return RSWA_EINVAL;
+  // grid limits of the block kernels: B sequences on grid.y, block * H
+  // queries on grid.x
+  if (block < 1 || block > (int64_t(1) << 24) || cache->cv.B > 65535 ||
+      block * cache->cv.H >= (int64_t(1) << 31))
+    return RSWA_EINVAL;
   if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
       !aligned16(o))
     return RSWA_EINVAL;

@@ -2,12 +2,15 @@
 //
 // Output t_b + i (i = 0..k-1) attends to the prefix, to the outputs of its
 // window already in the cache, j in [max(0, t_b + i - n + 1), t_b), and to
-// block tokens 0..i (k <= n keeps every earlier block token inside the
-// window).  The attention kernel reads the ring before the append kernel
-// overwrites any slot; both run on the caller's stream in that order, the
-// append kernel waiting on the attention kernel's completion.
-// This is the shape of a speculative-verification forward or of chunked
-// prefill of output text into an existing cache.
+// the block tokens of its window, i' in [max(0, i - n + 1), i].  The
+// attention kernel (here on the CUDA cores, or block_tc.cu on the tensor
+// cores) reads the ring before the append kernel overwrites any slot; both
+// run on the caller's stream in that order, the append kernel waiting on the
+// attention kernel's completion.  This is the shape of a
+// speculative-verification forward or of chunked prefill of output text into
+// an existing cache.
+#include <algorithm>
+
 #include "attend.cuh"
 
 namespace rswa {
@@ -66,11 +69,12 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
       attend_range<T, D>(qf, Kr, Vr, D, 0, a + cnt - n, first, step, -1, nullptr,
                          nullptr, lane, st);
   }
-  // block tokens 0..i (rows of the input, stride H_kv * D)
+  // block tokens of the window, max(0, i - n + 1) .. i (rows of the input,
+  // stride H_kv * D)
   const T* Kk = kblk + ((size_t)b * k * cv.Hkv + kvh) * D;
   const T* Vk = vblk + ((size_t)b * k * cv.Hkv + kvh) * D;
-  attend_range<T, D>(qf, Kk, Vk, row_stride, 0, i + 1, first, step, -1, nullptr,
-                     nullptr, lane, st);
+  attend_range<T, D>(qf, Kk, Vk, row_stride, max((int64_t)0, i - n + 1), i + 1,
+                     first, step, -1, nullptr, nullptr, lane, st);
   merge_groups<T, D>(st);
   __shared__ float s_m[NW], s_l[NW];
   __shared__ float s_acc[NW][D];
@@ -101,18 +105,20 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
   }
 }
 
-// One CTA per (block token i, sequence b): token i -> ring slot
-// (t_b + i) mod n for every KV head.  Each CTA reads t_b before it counts
-// itself done on the sequence's counter; the last of the k CTAs sets
-// t_b += k for every query head and rearms the counter.  The writes wait for
-// the attention kernel (programmatic dependent launch), which reads slots
-// that later block tokens overwrite.
+// One CTA per kept block token and sequence: the last kw = min(k, n) tokens
+// i = k - kw + blockIdx.x go to ring slot (t_b + i) mod n for every KV head
+// (earlier tokens of a longer block would be evicted by later ones).  Each
+// CTA reads t_b before it counts itself done on the sequence's counter; the
+// last of the kw CTAs sets t_b += k for every query head and rearms the
+// counter.  The writes wait for the attention kernel (programmatic dependent
+// launch), which reads slots that block tokens overwrite.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 append_block_kernel(CacheView cv, const T* __restrict__ kblk,
                     const T* __restrict__ vblk, int k) {
   griddep_wait();
-  const int i = blockIdx.x, b = blockIdx.y;
+  const int kw = (int)min((int64_t)k, cv.n);
+  const int i = k - kw + blockIdx.x, b = blockIdx.y;
   const int Hkv = cv.Hkv;                        // k, v carry the KV heads
   const int64_t t_b = cv.t_dev[(size_t)b * cv.H];
   constexpr int NV = D * (int)sizeof(T) / 16;
@@ -132,7 +138,7 @@ append_block_kernel(CacheView cv, const T* __restrict__ kblk,
   if (threadIdx.x == 0) {
     __threadfence();
     int32_t* cnt = cv.cnt_bh + (size_t)b * cv.H;
-    if (atomicAdd(cnt, 1) == k - 1) {
+    if (atomicAdd(cnt, 1) == kw - 1) {
       __threadfence();
       for (int h = 0; h < cv.H; ++h) cv.t_dev[(size_t)b * cv.H + h] = t_b + k;
       *cnt = 0;
@@ -162,20 +168,24 @@ template <typename T, int D>
 static cudaError_t launch_block_t(const CacheView& cv, const void* q,
                                   const void* k, const void* v, int64_t block,
                                   void* o, float* lse, cudaStream_t s) {
-  const int64_t nq = block * cv.H;
-  const dim3 grid((unsigned)nq, (unsigned)cv.B);
-  cudaError_t e =
-      nq * cv.B <= cv.sms
-          ? launch_pdl(decode_block_kernel<T, D, kBlockWarpsWide>, grid,
-                       dim3(kBlockWarpsWide * 32), s, cv, (const T*)q, (const T*)k,
-                       (const T*)v, block, (T*)o, lse)
-          : launch_pdl(decode_block_kernel<T, D, kBlockWarps>, grid,
-                       dim3(kBlockWarps * 32), s, cv, (const T*)q, (const T*)k,
-                       (const T*)v, block, (T*)o, lse);
+  cudaError_t e;
+  if (block_tc_supported(cv, block)) {
+    e = launch_block_tc(cv, q, k, v, block, o, lse, s);
+  } else {
+    const int64_t nq = block * cv.H;
+    const dim3 grid((unsigned)nq, (unsigned)cv.B);
+    e = nq * cv.B <= cv.sms
+            ? launch_pdl(decode_block_kernel<T, D, kBlockWarpsWide>, grid,
+                         dim3(kBlockWarpsWide * 32), s, cv, (const T*)q, (const T*)k,
+                         (const T*)v, block, (T*)o, lse)
+            : launch_pdl(decode_block_kernel<T, D, kBlockWarps>, grid,
+                         dim3(kBlockWarps * 32), s, cv, (const T*)q, (const T*)k,
+                         (const T*)v, block, (T*)o, lse);
+  }
   if (e != cudaSuccess) return e;
-  return launch_pdl(append_block_kernel<T, D>,
-                    dim3((unsigned)block, (unsigned)cv.B), dim3(128), s, cv,
-                    (const T*)k, (const T*)v, (int)block);
+  const int64_t kw = std::min<int64_t>(block, cv.n);
+  return launch_pdl(append_block_kernel<T, D>, dim3((unsigned)kw, (unsigned)cv.B),
+                    dim3(128), s, cv, (const T*)k, (const T*)v, (int)block);
 }
 
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,

@@ -105,6 +105,14 @@ cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
                                 const void* v, int64_t block, void* o, float* lse,
                                 cudaStream_t s);
+// Blocks of at least kBlockTcMin tokens of a bf16, head_dim 128 cache run
+// their attention on the tensor cores (block_tc.cu); smaller blocks, and
+// other caches, one CTA per query on the CUDA cores (decode_block.cu).
+constexpr int64_t kBlockTcMin = 16;
+bool block_tc_supported(const CacheView& cv, int64_t block);
+cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
+                            const void* v, int64_t block, void* o, float* lse,
+                            cudaStream_t s);
 // prefetch_prefix: the preceding kernel of the stream writes no prefix row
 // and no m_b of this cache (every decode launch but the first after a
 // prefill); the cluster path then loads them before its dependency wait.

@@ -188,3 +188,76 @@ def test_gqa_tc_back_to_back(cuda_lib):
             assert_close(got[b], ro, 1, f"step {s} seq {b}")
     for b in range(B):
         assert cache.get_t(b) == T + steps
+
+
+# ---------------------------------------------------------------------------
+# blocks of consecutive outputs, also longer than the window (chunked prefill
+# of output text into an existing cache)
+# ---------------------------------------------------------------------------
+
+CHUNK_CASES = [
+    # (m_list, n, H, Hkv, d, dtype, t0, blocks)  t0 outputs decoded first
+    ([288], 128, 10, 10, 128, 1, 0, [129]),                  # n + 1, empty ring
+    ([288], 128, 10, 10, 128, 1, 37, [391, 16]),             # 3n + 7, then 16
+    ([1056], 128, 4, 4, 128, 1, 200, [1000]),                # the ring wrapped
+    ([0], 128, 4, 4, 128, 1, 5, [1000, 129]),                # vanilla SWA
+    ([288, 0, 1056], 128, 4, 2, 128, 1, 130, [300]),         # ragged, grouped
+    ([300], 64, 3, 3, 128, 1, 20, [17, 64, 65]),             # tensor-core sizes
+    ([100], 7, 2, 2, 64, 1, 3, [20, 9]),                     # d 64: CUDA cores
+    ([50], 16, 2, 2, 128, 0, 9, [40]),                       # float32: CUDA cores
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CASES,
+                         ids=lambda c: f"m{c[0]}n{c[1]}H{c[2]}kv{c[3]}d{c[4]}t{c[6]}b{c[7]}")
+def test_decode_block_any_length(cuda_lib, case):
+    """A block of C outputs through rswa_decode_block equals rows
+    m + t0 .. m + t0 + C - 1 of the oracle's prefill of the whole sequence;
+    afterwards the ring holds the oracle's last n outputs bit-exactly and t_b
+    has advanced by C."""
+    rswa = cuda_lib
+    m_list, n, H, Hkv, d, dtype, t0, blocks = case
+    B = len(m_list)
+    dt = tdt(dtype)
+    T = t0 + sum(blocks)
+    rows = [m + T for m in m_list]
+    Q = workloads.normal((sum(rows), H, d), 401, 1.0, dt)
+    K = workloads.normal((sum(rows), Hkv, d), 402, 1.0, dt)
+    V = workloads.normal((sum(rows), Hkv, d), 403, 1.0, dt)
+    offs = np.cumsum([0] + rows)
+    seq = [slice(offs[b], offs[b + 1]) for b in range(B)]
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, dtype, kv_heads=Hkv)
+    # the prefix and the first t0 outputs by prefill
+    pk = torch.cat([K[s][:m + t0] for s, m in zip(seq, m_list)]).cuda()
+    pv = torch.cat([V[s][:m + t0] for s, m in zip(seq, m_list)]).cuda()
+    cache.prefill(None, pk, pv, None, m_list, t0)
+    refs = [oracle.prefill_attention(f64(Q[s]), f64(K[s]), f64(V[s]), m, n)
+            for s, m in zip(seq, m_list)]
+    t = t0
+    for C in blocks:
+        q, k, v = (torch.stack([x[s][m + t:m + t + C] for s, m in zip(seq, m_list)])
+                   .contiguous().cuda() for x in (Q, K, V))
+        o = torch.empty_like(q)
+        lse = torch.empty(B, C, H, device="cuda")
+        cache.decode_block(q, k, v, o, lse)
+        torch.cuda.synchronize()
+        for b, m in enumerate(m_list):
+            assert_close(f64(o[b]), refs[b][0][m + t:m + t + C], dtype,
+                         f"block at t={t} seq {b}")
+            assert np.abs(f64(lse[b]) - refs[b][1][m + t:m + t + C]).max() <= \
+                (1e-4 if dtype == 0 else 1e-3)
+        t += C
+        for b in range(B):
+            assert cache.get_t(b) == t
+    assert cache.sync_status() == 0
+    Ks, Vs = cache.slabs()
+    m_cap = max(m_list)
+    for b, (s, m) in enumerate(zip(seq, m_list)):
+        st = oracle.prefill_cache(f64(K[s]), f64(V[s]), m, n, T)
+        held = sorted(oracle.ring_outputs(T, n))
+        np.testing.assert_array_equal(
+            f64(Ks[b, :, m_cap:])[:, held].transpose(1, 0, 2), st["Kr"][held])
+        np.testing.assert_array_equal(
+            f64(Vs[b, :, m_cap:])[:, held].transpose(1, 0, 2), st["Vr"][held])
+        np.testing.assert_array_equal(f64(Ks[b, :, :m]).transpose(1, 0, 2), st["Kp"])
+        assert cache.cache_len(b) == oracle.cache_len(m, n, T)

@@ -297,8 +297,8 @@ def test_bf16_decode_block(cuda_lib, case):
             assert cache.get_t(b) == t
     assert cache.sync_status() == 0
     with pytest.raises(rswa.RswaError):
-        big = torch.zeros(B, n + 1, H, d, dtype=torch.bfloat16, device="cuda")
-        cache.decode_block(big, big, big, big)
+        empty = torch.zeros(B, 0, H, d, dtype=torch.bfloat16, device="cuda")
+        cache.decode_block(empty, empty, empty, empty)     # block 0
 
 
 def test_ring_sentinels_bit_exact(cuda_lib):
