@@ -218,7 +218,7 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
  * block == 1 runs rswa_decode_step_fused (same layouts), so the prefix
  * ordering rule of rswa_decode_step holds for every block size.  Larger
  * blocks take two kernels on `stream`: attention (on the tensor cores for
- * bf16, head_dim 128 and blocks of 16 or more; else on the CUDA cores), then
+ * bf16, head_dim 128 and blocks of 64 or more; else on the CUDA cores), then
  * the append, which waits for the attention kernel to finish (the ring
  * slots it overwrites are read by the block's earlier outputs).
  * Errors: RSWA_EINVAL (block outside 1..2^24, batch above 65535, null or
@@ -316,6 +316,17 @@ RSWA_API int rswa_sync_status(rswa_cache* cache);
  * involved.
  */
 RSWA_API void rswa_debug_fail_next_cuda(int count);
+
+/*
+ * Test hook: bound, in nanoseconds, on each wait of the tensor-core prefill
+ * and block-decode kernels for a pipeline phase (a tile landing, a tensor
+ * core result, a softmax hand-off); 0 restores the default of one second.
+ * Kernels launched with a bound that runs out stop, drain their own copies
+ * and tensor-core work (those waits keep the default bound), free their
+ * tensor memory and set the device flag that rswa_sync_status() reports as
+ * RSWA_EDEVICE.  Applies to launches made after the call; process-wide.
+ */
+RSWA_API void rswa_debug_set_wait_limit_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,8 @@ __all__ = [
     "rswa_decode_step", "rswa_decode_step_fused",
     "rswa_decode_step_fused_static", "rswa_decode_block", "rswa_cache_bytes",
     "rswa_cache_len", "rswa_cache_get_t", "rswa_cache_set_t",
-    "rswa_sync_status", "rswa_debug_fail_next_cuda", "rswa_cache_kv_offsets",
+    "rswa_sync_status", "rswa_debug_fail_next_cuda",
+    "rswa_debug_set_wait_limit_ns", "rswa_cache_kv_offsets",
     "RswaCache",
 ]
 
@@ -72,6 +73,7 @@ _SIGNATURES = {
     "rswa_cache_kv_offsets": (_c_int, [_c_vp, ctypes.POINTER(_c_size),
                                        ctypes.POINTER(_c_size)]),
     "rswa_debug_fail_next_cuda": (None, [_c_int]),
+    "rswa_debug_set_wait_limit_ns": (None, [ctypes.c_uint64]),
 }
 
 
@@ -142,6 +144,10 @@ def rswa_strerror(status: int) -> str:
 
 def rswa_debug_fail_next_cuda(count: int) -> None:
     load().rswa_debug_fail_next_cuda(count)
+
+
+def rswa_debug_set_wait_limit_ns(ns: int) -> None:
+    load().rswa_debug_set_wait_limit_ns(int(ns))
 
 
 def rswa_cache_footprint(m, n, heads, head_dim, batch, dtype) -> int:

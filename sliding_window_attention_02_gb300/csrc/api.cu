@@ -28,6 +28,7 @@ namespace {
 std::mutex g_mu;
 std::unordered_set<rswa_cache*> g_live;
 std::atomic<int> g_fail_next{0};
+std::atomic<uint64_t> g_wait_limit_ns{0};      // 0: the default bound
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -181,6 +182,11 @@ Layout make_layout(int64_t m, int64_t n, int heads, int kv_heads, int head_dim,
 
 }  // namespace
 
+uint64_t rswa::phase_wait_limit_ns() {
+  const uint64_t ns = g_wait_limit_ns.load();
+  return ns ? ns : 1000000000ull;
+}
+
 extern "C" {
 
 const char* rswa_strerror(int status) {
@@ -197,6 +203,8 @@ const char* rswa_strerror(int status) {
 }
 
 void rswa_debug_fail_next_cuda(int count) { g_fail_next.store(count < 0 ? 0 : count); }
+
+void rswa_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns); }
 
 int rswa_cache_footprint_gqa(int64_t m, int64_t n, int heads, int kv_heads,
                              int head_dim, int batch, int dtype,

@@ -120,13 +120,16 @@ __device__ __forceinline__ Unit unit_at(int u, const CacheView& cv, int C) {
   return w;
 }
 
+// wait_ns bounds every wait for a pipeline phase (phase_wait_limit_ns());
+// the drains before exit keep kWaitLimitNs.
 __global__ void __launch_bounds__(kThreads, 1)
 block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmKc,
                 const __grid_constant__ CUtensorMap tmVc,
                 const __grid_constant__ CUtensorMap tmKb,
                 const __grid_constant__ CUtensorMap tmVb, CacheView cv, int C,
-                __nv_bfloat16* __restrict__ O, float* __restrict__ lse) {
+                __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
+                uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -179,7 +182,7 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       for (; gi < 2u * (uint32_t)nt; ++gi) {
         const uint32_t s = gi % NS;
         if (gi >= (uint32_t)NS &&
-            !mbar_wait(bar(B_EMPTY + s), ((gi / NS) - 1) & 1, abort_flag, kWaitLimitNs))
+            !mbar_wait(bar(B_EMPTY + s), ((gi / NS) - 1) & 1, abort_flag, wait_ns))
           break;
         int kind, idx;
         w.tl.at((int)(gi >> 1), kind, idx);
@@ -211,7 +214,7 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, HD, true);
       auto wait = [&](int k, uint32_t phase) {
-        return mbar_wait(bar(k), phase & 1, abort_flag, kWaitLimitNs);
+        return mbar_wait(bar(k), phase & 1, abort_flag, wait_ns);
       };
       auto wait_slot = [&](uint32_t gi) { return wait(B_FULL + gi % NS, gi / NS); };
       auto qk = [&](int half, uint32_t gi) {
@@ -277,10 +280,12 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t o_addr = tmem + lane_off + tm_o(half);
     const int qh = w.q0 + half * BM;                    // first row of half
     const int i = qh + r;                               // row in the block
-    const int64_t n = cv.n;
-    // Ring: slot s is a key of row i iff its age a_s <= lim.
-    const int64_t lim = min(w.t_b - 1, n - 2 - (int64_t)i);
-    const int64_t r0 = w.t_b > 0 ? (w.t_b - 1) % n : 0;  // slot of output t_b - 1
+    const int n = (int)min(cv.n, (int64_t)1 << 30);
+    const int m_b = (int)w.m_b;
+    // Ring: slot s is a key of row i iff its age (r0 - s) mod n <= lim, i.e.
+    // s in [r0 - lim, r0] taken mod n (r0: slot of output t_b - 1).
+    const int lim = (int)min(w.t_b - 1, (int64_t)n - 2 - i);
+    const int r0 = w.t_b > 0 ? (int)((w.t_b - 1) % n) : 0;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
@@ -289,30 +294,45 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       const int k0 = idx * BN;
       // Tile fully visible for every row of this half.
       const bool full =
-          kind == kPrefix ? (int64_t)k0 + BN <= w.m_b
+          kind == kPrefix ? k0 + BN <= m_b
                           : (kind == kBlock && k0 + BN - 1 <= qh && k0 > qh + BM - 1 - n &&
                              k0 + BN <= C);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + half), j & 1, abort_flag,
-                                             kWaitLimitNs))) {
+                                             wait_ns))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      auto visible = [&](int c) -> bool {
-        const int64_t key = (int64_t)k0 + c;
-        if (kind == kPrefix) return key < w.m_b;
-        if (kind == kBlock) return key <= i && key > i - n && key < C;
-        if (key >= n) return false;
-        const int64_t age = key <= r0 ? r0 - key : r0 - key + n;
-        return age <= lim;
-      };
+      // This row's keys in the tile: columns [a1, b1] and [a2, b2].
+      int a1, b1, a2 = 1, b2 = 0;
+      if (kind == kPrefix) {
+        a1 = 0;
+        b1 = m_b - 1 - k0;
+      } else if (kind == kBlock) {
+        a1 = max(i - n + 1, 0) - k0;
+        b1 = min(i, C - 1) - k0;
+      } else if (lim < 0) {
+        a1 = 1;
+        b1 = 0;
+      } else if (r0 >= lim) {
+        a1 = r0 - lim - k0;
+        b1 = r0 - k0;
+      } else {
+        a1 = -k0;
+        b1 = r0 - k0;
+        a2 = r0 - lim + n - k0;
+        b2 = n - 1 - k0;
+      }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       uint32_t va[32], vb[32];
       auto max_chunk = [&](uint32_t* v, int c0) {
         if (!full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!visible(c0 + e)) v[e] = 0xff800000u;  // -inf
+          for (int e = 0; e < 32; ++e) {
+            const int c = c0 + e;
+            if (!((c >= a1 && c <= b1) || (c >= a2 && c <= b2)))
+              v[e] = 0xff800000u;                          // -inf
+          }
           tmem_st32(s_addr + c0, v);
         }
 #pragma unroll
@@ -402,7 +422,7 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
     // Epilogue: O / l -> bf16 -> global; lse in natural log units.
     if (ok && __all_sync(0xffffffffu,
-                         mbar_wait(bar(B_O + half), 0, abort_flag, kWaitLimitNs))) {
+                         mbar_wait(bar(B_O + half), 0, abort_flag, wait_ns))) {
       tc_fence_after();
       const float inv = 1.f / l_run;
       const size_t row = (size_t)w.b * C + i;
@@ -464,7 +484,8 @@ cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
   if (e != cudaSuccess) return e;
   const int64_t units = (int64_t)cv.B * ((C + 2 * BM - 1) / (2 * BM)) * cv.H;
   block_tc_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(
-      mq, mkc, mvc, mkb, mvb, cv, C, static_cast<__nv_bfloat16*>(o), lse);
+      mq, mkc, mvc, mkb, mvb, cv, C, static_cast<__nv_bfloat16*>(o), lse,
+      phase_wait_limit_ns());
   return cudaGetLastError();
 }
 

@@ -165,6 +165,8 @@ __device__ __forceinline__ Unit unit_at(int u, const CacheView& cv,
   return w;
 }
 
+// wait_ns bounds every wait for a pipeline phase (phase_wait_limit_ns());
+// the drains before exit keep kWaitLimitNs.
 // PERSIST: a CTA may take several units (one per round of gridDim units)
 // and skips (query tile, key tile) products the mask excludes entirely;
 // otherwise exactly one unit, blockIdx.x, the cross-unit barriers (B_QFREE,
@@ -175,7 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, CacheView cv,
-                  SeqTable st, __nv_bfloat16* __restrict__ O, int total_pairs) {
+                  SeqTable st, __nv_bfloat16* __restrict__ O, int total_pairs,
+                  uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,7 +227,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const Unit w = unit_at(u, cv, st, total_pairs);
         if (w.tr.nt == 0) continue;
         // Q of the previous unit is read by its last QK MMA.
-        if (nq > 0 && !mbar_wait(bar(B_QFREE), (nq - 1) & 1, abort_flag, kWaitLimitNs))
+        if (nq > 0 && !mbar_wait(bar(B_QFREE), (nq - 1) & 1, abort_flag, wait_ns))
           break;
         const int x0 = w.h * HD;                               // Q column
         const int xk = w.kvh * HD;                             // K, V column
@@ -239,7 +242,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           const uint32_t s = gi % NS;
           if (gi >= (uint32_t)NS &&
               !mbar_wait(bar(B_EMPTY + s), ((gi / NS) - 1) & 1, abort_flag,
-                         kWaitLimitNs)) {
+                         wait_ns)) {
             ok = false;
             break;
           }
@@ -263,7 +266,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, HD, true);
       auto wait = [&](int k, uint32_t phase) {
-        return mbar_wait(bar(k), phase & 1, abort_flag, kWaitLimitNs);
+        return mbar_wait(bar(k), phase & 1, abort_flag, wait_ns);
       };
       auto wait_slot = [&](uint32_t gi) { return wait(B_FULL + gi % NS, gi / NS); };
       // S_h = Q_h K^T from the K tile in the ring slot of load gi.
@@ -443,7 +446,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         // The warp agrees on the outcome, so no lane reaches the warp-wide
         // TMEM loads alone.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S + half), (gt + j) & 1,
-                                               abort_flag, kWaitLimitNs))) {
+                                               abort_flag, wait_ns))) {
           ok = false;
           break;
         }
@@ -566,7 +569,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
       if (!ok) break;
       // Epilogue: O / l -> bf16 -> global, then O_h is free for the next unit.
       if (!__all_sync(0xffffffffu,
-                      mbar_wait(bar(B_O + half), kq & 1, abort_flag, kWaitLimitNs)))
+                      mbar_wait(bar(B_O + half), kq & 1, abort_flag, wait_ns)))
         break;
       tc_fence_after();
       const float inv = 1.f / l_run;
@@ -718,12 +721,13 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
     if (e != cudaSuccess) return e;
     grid = std::min<int64_t>(units, std::max(sms, 1));
   }
+  const uint64_t wait_ns = phase_wait_limit_ns();
   if (persist)
     prefill_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
   else
     prefill_tc_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs);
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
   return cudaGetLastError();
 }
 

@@ -52,6 +52,10 @@ struct SeqTable {
   int32_t tile_off[kMaxSeqPerLaunch + 1];// cumulative 128-row q-tiles
 };
 
+// Bound on the tensor-core prefill and block kernels' waits for a pipeline
+// phase: 1 s, or what rswa_debug_set_wait_limit_ns set (test hook).
+uint64_t phase_wait_limit_ns();
+
 // ---- launchers (each returns the cudaError_t of its launch) ----
 cudaError_t launch_prefill_cache(const CacheView& cv, const SeqTable& st,
                                  const void* K, const void* V, int64_t max_rows,
@@ -107,8 +111,10 @@ cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* 
                                 cudaStream_t s);
 // Blocks of at least kBlockTcMin tokens of a bf16, head_dim 128 cache run
 // their attention on the tensor cores (block_tc.cu); smaller blocks, and
-// other caches, one CTA per query on the CUDA cores (decode_block.cu).
-constexpr int64_t kBlockTcMin = 16;
+// other caches, one CTA per query on the CUDA cores (decode_block.cu), which
+// measured faster below 64 tokens on GB300 (single-page cache, 16 tokens:
+// 12.3 against ~30 us).
+constexpr int64_t kBlockTcMin = 64;
 bool block_tc_supported(const CacheView& cv, int64_t block);
 cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
                             const void* v, int64_t block, void* o, float* lse,

@@ -53,14 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait: gives up after `limit_ns` (or at once when *abort is set),
-// raising *abort so that every other role stops waiting too.
+// raising *abort so that every other role stops waiting too.  The clock and
+// the flag are checked after the second failed poll and every 64 polls
+// after it.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if ((it & 63u) == 1) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
