@@ -4,8 +4,8 @@
 // for an output row (i >= m), to the window [max(m, i - n + 1), i]
 // ("Unlimited-OCR deep dive", N(t) = P U D_n(t)).  The two key ranges are
 // streamed with the same warp routine as the decode step.  This kernel serves
-// float32 caches (where tensor-core tf32 would not hold float32 accuracy) and
-// head_dim 64; bf16 head_dim 128 runs on the tcgen05 kernel.
+// float32 caches (where tensor-core tf32 would not hold float32 accuracy);
+// bf16 caches run on the tcgen05 kernel.
 #include "attend.cuh"
 
 namespace rswa {

@@ -51,7 +51,7 @@ using namespace ptx;
 
 constexpr int BM = 128;                        // rows per half
 constexpr int BN = 128;                        // keys per tile
-constexpr int HD = 128;                        // head_dim
+constexpr int HD = 128;                        // largest head_dim (smem layout)
 constexpr int kSoftmaxThreads = 256;
 constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
@@ -165,6 +165,12 @@ __device__ __forceinline__ Unit unit_at(int u, const CacheView& cv,
   return w;
 }
 
+// Tile bytes of a head_dim-D operand: D / 64 swizzle atoms of 128 rows.
+template <int D>
+constexpr uint32_t tile_bytes() { return (uint32_t)(D / 64) * kSub; }
+
+// D: head_dim, 64 or 128 (one or two 64-column atoms per Q/K/V tile; the
+// shared-memory layout is the head_dim-128 one either way).
 // wait_ns bounds every wait for a pipeline phase (phase_wait_limit_ns());
 // the drains before exit keep kWaitLimitNs.
 // PERSIST: a CTA may take several units (one per round of gridDim units)
@@ -172,7 +178,7 @@ __device__ __forceinline__ Unit unit_at(int u, const CacheView& cv,
 // otherwise exactly one unit, blockIdx.x, the cross-unit barriers (B_QFREE,
 // B_OFREE) and phase counters fold away, and every product of the unit's
 // tile list runs.
-template <bool PERSIST>
+template <bool PERSIST, int D>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                   const __grid_constant__ CUtensorMap tmK,
@@ -229,14 +235,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         // Q of the previous unit is read by its last QK MMA.
         if (nq > 0 && !mbar_wait(bar(B_QFREE), (nq - 1) & 1, abort_flag, wait_ns))
           break;
-        const int x0 = w.h * HD;                               // Q column
-        const int xk = w.kvh * HD;                             // K, V column
+        const int x0 = w.h * D;                                // Q column
+        const int xk = w.kvh * D;                              // K, V column
         const int yq = (int)(w.row0 + w.q0);
-        mbar_arrive_expect_tx(bar(B_Q), 2 * kTileB);
+        mbar_arrive_expect_tx(bar(B_Q), 2 * tile_bytes<D>());
         tma_load_2d(sb + OFF_Q, &tmQ, x0, yq, bar(B_Q));
-        tma_load_2d(sb + OFF_Q + kSub, &tmQ, x0 + 64, yq, bar(B_Q));
+        if (D > 64) tma_load_2d(sb + OFF_Q + kSub, &tmQ, x0 + 64, yq, bar(B_Q));
         tma_load_2d(sb + OFF_Q + kTileB, &tmQ, x0, yq + BM, bar(B_Q));
-        tma_load_2d(sb + OFF_Q + kTileB + kSub, &tmQ, x0 + 64, yq + BM, bar(B_Q));
+        if (D > 64) tma_load_2d(sb + OFF_Q + kTileB + kSub, &tmQ, x0 + 64, yq + BM, bar(B_Q));
         ++nq;
         for (int idx = 0; idx < 2 * w.tr.nt; ++idx, ++gi) {
           const uint32_t s = gi % NS;
@@ -249,9 +255,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
           const CUtensorMap* map = (idx & 1) ? &tmV : &tmK;
           const int y = (int)(w.row0 + (int64_t)tile_at(w.tr, idx >> 1) * BN);
           const uint32_t dst = sb + OFF_RING + s * kTileB;
-          mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
+          mbar_arrive_expect_tx(bar(B_FULL + s), tile_bytes<D>());
           tma_load_2d(dst, map, xk, y, bar(B_FULL + s));
-          tma_load_2d(dst + kSub, map, xk + 64, y, bar(B_FULL + s));
+          if (D > 64) tma_load_2d(dst + kSub, map, xk + 64, y, bar(B_FULL + s));
         }
       }
       // Drain: every copy issued has landed before the CTA may exit (older
@@ -264,7 +270,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(BM, HD, true);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, true);
       auto wait = [&](int k, uint32_t phase) {
         return mbar_wait(bar(k), phase & 1, abort_flag, wait_ns);
       };
@@ -274,7 +280,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const uint32_t kb = sb + OFF_RING + (gi % NS) * kTileB;
         const uint32_t qb = sb + OFF_Q + half * kTileB;
 #pragma unroll
-        for (int k = 0; k < HD / 16; ++k) {
+        for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
           mma_bf16_ss(tmem + tm_s(half), desc_sw128(qb + off, 16, 1024),
                       desc_sw128(kb + off, 16, 1024), idesc_qk, k > 0);
@@ -422,7 +428,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int half = warp >> 2;
     const int r = threadIdx.x & 127;                    // row in half
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const float sl2 = rsqrtf((float)HD) * kLog2e;
+    const float sl2 = rsqrtf((float)D) * kLog2e;
     const uint32_t s_addr = tmem + lane_off + tm_s(half);
     const uint32_t o_addr = tmem + lane_off + tm_o(half);
     uint32_t gt = 0, kq = 0;                            // tiles, units done
@@ -513,7 +519,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         const float nref = (m_run == -INFINITY) ? 0.f : -m_run;
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32_sync(o_addr + c * 32, o);
 #pragma unroll
@@ -573,9 +579,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
         break;
       tc_fence_after();
       const float inv = 1.f / l_run;
-      __nv_bfloat16* orow = O + ((w.row0 + i) * H + w.h) * HD;
+      __nv_bfloat16* orow = O + ((w.row0 + i) * H + w.h) * D;
 #pragma unroll 1
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32_sync(o_addr + c * 32, o);
         if (i < w.L) {
@@ -628,10 +634,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [rows][heads*128] bf16 viewed as a 2-D tensor; box 64 columns x 128 rows,
+// [rows][heads*d] bf16 viewed as a 2-D tensor; box 64 columns x 128 rows,
 // 128-byte swizzle; rows past `rows` read as zero.
-bool make_map(CUtensorMap* map, const void* base, int H, int64_t rows) {
-  return make_tmap_rows_bf16(map, base, (uint64_t)H * HD, (uint64_t)rows);
+bool make_map(CUtensorMap* map, const void* base, int H, int d, int64_t rows) {
+  return make_tmap_rows_bf16(map, base, (uint64_t)H * d, (uint64_t)rows);
 }
 
 }  // namespace
@@ -674,7 +680,30 @@ static int64_t host_tiles(const SeqTable& st, int64_t n_window) {
 }
 
 bool prefill_tc_supported(const CacheView& cv) {
-  return cv.dtype == RSWA_BF16 && cv.d == HD && encode_fn() != nullptr;
+  return cv.dtype == RSWA_BF16 && (cv.d == 64 || cv.d == 128) && encode_fn() != nullptr;
+}
+
+template <int D>
+static cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CacheView& cv,
+                            const SeqTable& st, void* O, int pairs, bool persist,
+                            int64_t grid, cudaStream_t s) {
+  // Per device (the attribute belongs to the current device's context).
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_tc_kernel<false, D>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const uint64_t wait_ns = phase_wait_limit_ns();
+  if (persist)
+    prefill_tc_kernel<true, D><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
+  else
+    prefill_tc_kernel<false, D><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
+        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
@@ -684,17 +713,9 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
   const int64_t end_row = st_in.row_off[0] + total_rows;
   if (end_row >= (int64_t(1) << 31)) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, Q, cv.H, end_row) || !make_map(&mk, K, cv.Hkv, end_row) ||
-      !make_map(&mv, V, cv.Hkv, end_row))
+  if (!make_map(&mq, Q, cv.H, cv.d, end_row) || !make_map(&mk, K, cv.Hkv, cv.d, end_row) ||
+      !make_map(&mv, V, cv.Hkv, cv.d, end_row))
     return cudaErrorInvalidValue;
-  // Per device (the attribute belongs to the current device's context).
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_tc_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
   // Work units are pairs of 128-row tiles: tile_off counts pairs here.
   SeqTable st = st_in;
   int pairs = 0;
@@ -711,24 +732,10 @@ cudaError_t launch_prefill_tc(const CacheView& cv, const SeqTable& st_in,
   // tiles (band-dominated sequences) run persistently, one unit per round of
   // gridDim units, so that the next unit's loads overlap this one's tail;
   // long units run one per CTA, left to the hardware's dynamic scheduling.
-  int64_t grid = units;
   const bool persist = host_tiles(st, cv.n) < kPersistentTilesPerUnit * pairs;
-  if (persist) {
-    int dev = 0, sms = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    grid = std::min<int64_t>(units, std::max(sms, 1));
-  }
-  const uint64_t wait_ns = phase_wait_limit_ns();
-  if (persist)
-    prefill_tc_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
-  else
-    prefill_tc_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(
-        mq, mk, mv, cv, st, static_cast<__nv_bfloat16*>(O), pairs, wait_ns);
-  return cudaGetLastError();
+  const int64_t grid = persist ? std::min<int64_t>(units, std::max(cv.sms, 1)) : units;
+  if (cv.d == 64) return launch_d<64>(mq, mk, mv, cv, st, O, pairs, persist, grid, s);
+  return launch_d<128>(mq, mk, mv, cv, st, O, pairs, persist, grid, s);
 }
 
 }  // namespace rswa

@@ -144,6 +144,12 @@ PREFILL_CASES = [
     ([40, 0, 133], 16, 37, 2, 128),
     ([200, 7], 128, 300, 1, 128),
     ([10], 4000, 300, 1, 128),   # n >= T: plain causal attention
+    # head_dim 64 on the tensor cores: short units (persistent launch), long
+    # units (one per CTA), ragged sequences, grouped heads via test_gqa_prefill
+    ([0], 128, 1000, 2, 64),
+    ([3000], 128, 500, 2, 64),
+    ([40, 0, 133, 700], 16, 37, 3, 64),
+    ([1], 1, 1, 1, 64),
 ]
 
 
