@@ -50,6 +50,7 @@ KERNEL_SOURCES = {
     "decode_gqa_tc_kernel": ["decode_gqa_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
     "decode_stream_kernel": ["decode_stream.cu", "attend.cuh", "rswa_device.cuh",
                              "tc_ptx.cuh"],
+    "block_tc_kernel": ["block_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
     "prefill_tc_kernel": ["prefill_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
 }
 
@@ -726,7 +727,7 @@ def run_extras(dev, peaks, quick=False):
     tf = flops / (ms * 1e-3) / 1e12
     out["prefill"] = {
         "workload": "B1 H10 d128 m10272 T22496 (32K) n128 bf16, %d layers" % layers,
-        "ms_per_step": round(ms, 3), "algorithmic_flops": flops,
+        "ms_per_step": round(ms, 3), "layers": layers, "algorithmic_flops": flops,
         "TFLOP_per_s": round(tf, 1),
         "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
         "frac_bf16_burst": round(tf / peaks["bf16_tflops"], 4)}
@@ -1006,11 +1007,14 @@ def extra_rooflines(extras, peaks, peak_src):
                                   "hbm_gbs", peak_src, "decode_kernel@batched"))
     pf = extras.get("prefill")
     if pf:
-        # 12 back-to-back layers, 13 ms: the burst peak applies
-        out.append(roofline_entry("prefill_tc_kernel", "multipage_prefill_bf16",
-                                  "tensor", pf["algorithmic_flops"],
-                                  1e3 * pf["ms_per_step"], peaks["bf16_tflops"],
-                                  "bf16_tflops", peak_src,
+        # per launch (one layer) of 12 back-to-back layers, 13 ms in all:
+        # the burst peak applies
+        layers = pf.get("layers", 12)
+        out.append(roofline_entry("prefill_tc_kernel", "multipage_prefill_bf16 "
+                                  "(per layer)", "tensor",
+                                  pf["algorithmic_flops"] // layers,
+                                  1e3 * pf["ms_per_step"] / layers,
+                                  peaks["bf16_tflops"], "bf16_tflops", peak_src,
                                   "prefill_tc_kernel@multipage"))
     lp = extras.get("long_prefix_decode")
     if lp:
@@ -1300,6 +1304,38 @@ def main_only(args):
 
         def step():
             st["cache"].decode_step_fused(q, k, v, o, stream=s)
+    elif args.only == "long_prefix":
+        import sliding_window_attention_02_gb300 as rswa
+        import workloads
+        H, d, n, m = 10, 128, 128, 10272          # one sequence, 40 pages
+        layers = args.layers or 2
+        caches = []
+        for layer in range(layers):
+            _, K, V = workloads.qkv(m + n, H, d, layer, 1.0, torch.bfloat16,
+                                    device=dev)
+            c = rswa.RswaCache(m, n, H, d, 1, rswa.RSWA_BF16, device=dev)
+            c.prefill(None, K, V, None, [m], n, stream=s)
+            caches.append(c)
+        q, k, v = workloads.qkv(1, H, d, 5, 1.0, torch.bfloat16, device=dev)
+        o = torch.empty(1, H, d, dtype=torch.bfloat16, device=dev)
+
+        def step():
+            for c in caches:
+                c.decode_step_fused(q, k, v, o, stream=s)
+    elif args.only == "block":
+        import sliding_window_attention_02_gb300 as rswa
+        import workloads
+        w = workloads.WORKLOADS["single_page_bf16"]
+        B, H, d, m, n = w.batch, w.heads, w.head_dim, w.m, w.n
+        C = args.block
+        Q, K, V = workloads.qkv(m + C, H, d, 0, w.std, torch.bfloat16, device=dev)
+        c = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, device=dev)
+        c.prefill(None, K[:m], V[:m], None, [m], 0, stream=s)
+        q, k, v = (x[m:m + C][None].contiguous() for x in (Q, K, V))
+        o = torch.empty_like(q)
+
+        def step():
+            c.decode_block(q, k, v, o, stream=s)
     elif args.only == "vanilla_prefill":
         import sliding_window_attention_02_gb300 as rswa
         import workloads
@@ -1353,11 +1389,13 @@ def main():
     ap.add_argument("--cpu-max-steps", type=int, default=None)
     ap.add_argument("--only", default=None,
                     choices=["single_page", "batched", "sweep", "gqa", "prefill",
-                             "vanilla_prefill"],
+                             "vanilla_prefill", "long_prefix", "block"],
                     help="run one workload warmup+steps times and print its "
                          "mean step time (for profiling)")
     ap.add_argument("--layers", type=int, default=None,
-                    help="prefill layers with --only prefill")
+                    help="layers with --only prefill or long_prefix")
+    ap.add_argument("--block", type=int, default=1024,
+                    help="tokens per call with --only block")
     args = ap.parse_args()
     if args.cpu_configs_worker:
         print(json.dumps(oracle_config_samples()))
