@@ -318,9 +318,11 @@ RSWA_API int rswa_sync_status(rswa_cache* cache);
 RSWA_API void rswa_debug_fail_next_cuda(int count);
 
 /*
- * Test hook: bound, in nanoseconds, on each wait of the tensor-core prefill
- * and block-decode kernels for a pipeline phase (a tile landing, a tensor
- * core result, a softmax hand-off); 0 restores the default of one second.
+ * Test hook: bound, in nanoseconds, on each wait for a pipeline phase (a
+ * tile landing, a tensor core result, a softmax hand-off) of the pipelined
+ * kernels - the tensor-core prefill, block decode and grouped-head decode,
+ * and the shared-memory streaming decode; 0 restores the default of one
+ * second.
  * Kernels launched with a bound that runs out stop, drain their own copies
  * and tensor-core work (those waits keep the default bound), free their
  * tensor memory and set the device flag that rswa_sync_status() reports as

@@ -28,8 +28,9 @@
 // Rows of a tile past the chunk's end are masked (score -inf, p = 0); the
 // cache's K/V regions are zeroed at creation, so such rows hold finite
 // values and contribute exactly 0.
-// Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
-// frees TMEM, sets the cache's device error flag and exits.
+// Every wait is bounded (wait_ns, phase_wait_limit_ns(), for the pipeline's
+// phases; kWaitLimitNs for the drains); on a timeout the CTA drains its
+// copies and MMAs, frees TMEM, sets the cache's device error flag and exits.
 #include <cuda.h>
 
 #include "rswa_device.cuh"
@@ -100,7 +101,8 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                      const __nv_bfloat16* __restrict__ q,
                      const __nv_bfloat16* __restrict__ knew,
                      const __nv_bfloat16* __restrict__ vnew,
-                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse) {
+                     __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                     uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,7 +286,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       int issued = first_loads;
       for (int idx = first_loads; idx < 2 * nt; ++idx) {
         if (!mbar_wait(bar(B_EMPTY + idx % NS), ((idx / NS) - 1) & 1, abort_flag,
-                       kWaitLimitNs))
+                       wait_ns))
           break;
         load(idx);
         ++issued;
@@ -304,7 +306,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
       constexpr uint32_t idesc_o = idesc_bf16_ab(HD, NQ, true, false);
       auto full = [&](int idx) {
         return mbar_wait(bar(B_FULL + idx % NS), (idx / NS) & 1, abort_flag,
-                         kWaitLimitNs);
+                         wait_ns);
       };
       // S^T(j) = K_j Q^T: A = K tile (K-major over d), B = Q^T.
       auto issue_s = [&](int j) {
@@ -331,14 +333,14 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
         mma_commit(bar(B_EMPTY + (2 * j + 1) % NS));
       };
       auto pv_ready = [&](int j) {
-        return mbar_wait(bar(B_P + (j & 1)), (j >> 1) & 1, abort_flag, kWaitLimitNs) &&
+        return mbar_wait(bar(B_P + (j & 1)), (j >> 1) & 1, abort_flag, wait_ns) &&
                full(2 * j + 1);
       };
       bool ok = live;
       for (int j = 0; ok && j < nt; ++j) {
         ok = full(2 * j) &&
              (j < 2 || mbar_wait(bar(B_SFREE + (j & 1)), ((j - 2) >> 1) & 1,
-                                 abort_flag, kWaitLimitNs));
+                                 abort_flag, wait_ns));
         if (!ok) break;
         tc_fence_after();
         issue_s(j);
@@ -364,12 +366,12 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     // softmax warps on an mbarrier: bounded, so a warp that gives up cannot
     // leave the others blocked.
     auto wait_all = [&](int k, uint32_t parity) {
-      return __all_sync(0xffffffffu, mbar_wait(bar(k), parity, abort_flag, kWaitLimitNs));
+      return __all_sync(0xffffffffu, mbar_wait(bar(k), parity, abort_flag, wait_ns));
     };
     int n_sync = 0;
     auto soft_sync = [&]() {
       mbar_arrive(bar(B_SYNC));
-      const bool r = mbar_wait(bar(B_SYNC), n_sync & 1, abort_flag, kWaitLimitNs);
+      const bool r = mbar_wait(bar(B_SYNC), n_sync & 1, abort_flag, wait_ns);
       ++n_sync;
       return __all_sync(0xffffffffu, r);
     };
@@ -449,7 +451,7 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   bool have_o = false;
   uint32_t ov[16];
   if (tid < kSoftThreads && live && nt > 0 && !*abort_flag &&
-      __all_sync(0xffffffffu, mbar_wait(bar(B_O), 0, abort_flag, kWaitLimitNs))) {
+      __all_sync(0xffffffffu, mbar_wait(bar(B_O), 0, abort_flag, wait_ns))) {
     tc_fence_after();
     tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + TM_O, ov);
     tmem_wait_ld();
@@ -535,7 +537,8 @@ cudaError_t launch_tc(const CacheView& cv, const CUtensorMap& mk,
   using BF = __nv_bfloat16;
   return cudaLaunchKernelEx(&cfg, kern, mk, mv, mk8, mv8, cv, (const BF*)q,
                             (const BF*)(FUSED ? k : nullptr),
-                            (const BF*)(FUSED ? v : nullptr), (BF*)o, lse);
+                            (const BF*)(FUSED ? v : nullptr), (BF*)o, lse,
+                            phase_wait_limit_ns());
 }
 
 template <bool FUSED, bool PREFETCH>

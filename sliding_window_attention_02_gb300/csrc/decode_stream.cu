@@ -23,8 +23,10 @@
 // the previous kernel of the stream drains; ring rows, t_b and q are read
 // after it.  Every CTA publishes (m, l, acc[d]); the last of the head's CTAs
 // to arrive (atomic counter) merges the partials and writes o, lse and
-// t_b + 1.  Every wait is bounded; on a timeout the CTA drains its copies,
-// publishes what it has, and sets the cache's device error flag.
+// t_b + 1.  Every wait is bounded (wait_ns, phase_wait_limit_ns(), for the
+// pipeline's phases; kWaitLimitNs for the drain); on a timeout the CTA
+// drains its copies, publishes what it has, and sets the cache's device
+// error flag.
 #include <algorithm>
 
 #include "attend.cuh"
@@ -77,7 +79,7 @@ template <typename T, int D, bool FUSED, bool PREFETCH>
 __global__ void __launch_bounds__(kThreads, (NS * kStageBytes <= 100 * 1024) ? 2 : 1)
 decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
                      const T* __restrict__ knew, const T* __restrict__ vnew,
-                     T* __restrict__ o, float* __restrict__ lse) {
+                     T* __restrict__ o, float* __restrict__ lse, uint64_t wait_ns) {
   using C = AttendCfg<T, D, kU>;
   constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW;
   constexpr uint32_t ROW_B = D * sizeof(T);            // bytes of a K or V row
@@ -127,7 +129,7 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
   auto issue = [&](int k) {
     const int s = k % NS;
     if (k >= NS && !ptx::mbar_wait(empty(s), ((k / NS) - 1) & 1, abort_flag,
-                                   kWaitLimitNs))
+                                   wait_ns))
       return false;
     const int64_t l0 = span0 + (int64_t)k * SR, l1 = min(l0 + SR, span1);
     const int64_t p1 = min(l1, m_b);                    // prefix rows [l0, p1)
@@ -208,7 +210,7 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     for (int k = 0; k < nst; ++k) {
       const int s = k % NS;
       if (!__all_sync(0xffffffffu, ptx::mbar_wait(full(s), (k / NS) & 1, abort_flag,
-                                                  kWaitLimitNs)))
+                                                  wait_ns)))
         break;
       const int64_t l0 = span0 + (int64_t)k * SR, l1 = min(l0 + SR, span1);
       const uint32_t kd = sb + (uint32_t)s * kStageBytes, vd = kd + kTensorStage;
@@ -315,7 +317,8 @@ cudaError_t launch_t(const CacheView& cv, int S, const void* q, const void* k,
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, cv, S, (const T*)q,
                             (const T*)(FUSED ? k : nullptr),
-                            (const T*)(FUSED ? v : nullptr), (T*)o, lse);
+                            (const T*)(FUSED ? v : nullptr), (T*)o, lse,
+                            phase_wait_limit_ns());
 }
 
 template <typename T, int D>

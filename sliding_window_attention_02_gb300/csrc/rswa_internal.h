@@ -52,8 +52,9 @@ struct SeqTable {
   int32_t tile_off[kMaxSeqPerLaunch + 1];// cumulative 128-row q-tiles
 };
 
-// Bound on the tensor-core prefill and block kernels' waits for a pipeline
-// phase: 1 s, or what rswa_debug_set_wait_limit_ns set (test hook).
+// Bound on the pipelined kernels' waits for a pipeline phase (tensor-core
+// prefill, block, grouped decode; streaming decode): 1 s, or what
+// rswa_debug_set_wait_limit_ns set (test hook).
 uint64_t phase_wait_limit_ns();
 
 // ---- launchers (each returns the cudaError_t of its launch) ----

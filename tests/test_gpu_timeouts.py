@@ -80,3 +80,35 @@ def test_block_wait_runs_out_then_recovers(cuda_lib):
                                       range(m + C, m + 2 * C))
     _close(f64(o[0]), ref, "block after the timeout")
     assert cache.get_t(0) == 2 * C
+
+
+@pytest.mark.parametrize("m,H,Hkv,B", [(10272, 10, 10, 1),      # streaming decode
+                                       (1400, 16, 4, 24)])      # grouped, tensor cores
+def test_decode_wait_runs_out_then_recovers(cuda_lib, m, H, Hkv, B):
+    """A fused decode step whose phase waits run out still appends its key
+    and value and advances t_b (every CTA publishes and arrives); the step
+    after it, with the default bound, matches the oracle."""
+    rswa = cuda_lib
+    d, n = 128, 128
+    K = workloads.normal((B * m, Hkv, d), 61, 1.0, torch.bfloat16)
+    V = workloads.normal((B * m, Hkv, d), 62, 1.0, torch.bfloat16)
+    cache = rswa.RswaCache(m, n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    cache.prefill(None, K.cuda(), V.cuda(), None, [m] * B, 0)
+    states = [oracle.prefill_cache(f64(K[b * m:(b + 1) * m]), f64(V[b * m:(b + 1) * m]),
+                                   m, n, 0) for b in range(B)]
+    steps = [tuple(workloads.normal((B, h, d), 63 + 3 * s + i, 1.0, torch.bfloat16).cuda()
+                   for i, h in enumerate((H, Hkv, Hkv))) for s in range(2)]
+    o = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    status = _timed_out(rswa, cache, lambda: cache.decode_step_fused(*steps[0], o))
+    assert status == RSWA_EDEVICE
+    for b in range(B):
+        assert cache.get_t(b) == 1
+    cache.decode_step_fused(*steps[1], o)
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    for b in range(B):
+        for s in range(2):
+            q, k, v = (f64(x[b]) for x in steps[s])
+            states[b], ro, _ = oracle.decode_step_fused(states[b], q, k, v, n)
+        _close(f64(o[b]), ro, f"seq {b} after the timeout")
+        assert cache.get_t(b) == 2
