@@ -284,8 +284,14 @@ RSWA_API int rswa_cache_get_t(rswa_cache* cache, int b, int64_t* out);
  * Restore t_b for every sequence (t_per_seq: HOST array of B values >= 0),
  * e.g. when resuming a saved cache.  The ring is taken to hold outputs
  * t_b - min(n, t_b) .. t_b - 1 in slots j mod n; the call rewrites no
- * key/value data.  Copies from host memory and synchronises the stream
- * before returning (not for use inside stream capture).
+ * key/value data.  It also clears the decode kernels' split-K arrival
+ * counters.  Copies from host memory and synchronises the stream before
+ * returning (not for use inside stream capture).
+ * After a decode step that reported RSWA_EDEVICE (rswa_sync_status), its
+ * outputs are undefined and t_b may be advanced for some heads and not for
+ * others, though the step's key and value were appended: call
+ * rswa_cache_set_t with the intended t_b (the old one + 1) before the next
+ * step.
  * Errors: RSWA_EINVAL, RSWA_ECUDA.
  */
 RSWA_API int rswa_cache_set_t(rswa_cache* cache, const int64_t* t_per_seq,

@@ -104,6 +104,10 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
 
 cudaError_t launch_set_t(const CacheView& cv, const int64_t* t_host,
                          cudaStream_t s) {
+  // A decode step that flagged an error may have left split-K arrival
+  // counters part-way: restoring t_b clears them too.
+  cudaError_t e = cudaMemsetAsync(cv.cnt_bh, 0, sizeof(int32_t) * (size_t)cv.B * cv.H, s);
+  if (e != cudaSuccess) return e;
   // One copy of t_b per head; the caller synchronises before t_host and this
   // staging array go away.
   static thread_local std::vector<int64_t> per_head;

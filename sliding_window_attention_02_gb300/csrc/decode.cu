@@ -581,6 +581,11 @@ static cudaError_t launch_decode_t(const CacheView& cv, const void* q,
 #ifndef RSWA_GQA_TC
 #define RSWA_GQA_TC 1
 #endif
+// 1: the stream-K form of the tensor-core grouped decode where it applies;
+// 0: one CTA per chunk of a KV head (decode_gqa_tc.cu).
+#ifndef RSWA_GQA_SK
+#define RSWA_GQA_SK 1
+#endif
 
 // The cluster path when every head's cache fits one row batch per CTA of a
 // cluster of at most 8 (longer caches are the split-K path's job) and all
@@ -595,6 +600,8 @@ cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
                           bool prefetch_prefix, cudaStream_t s) {
   const bool pf = prefetch_prefix;
   if (cv.H != cv.Hkv && !decode_use_small(cv)) {
+    if (RSWA_GQA_TC && RSWA_GQA_SK && gqa_sk_supported(cv))
+      return launch_decode_gqa_sk(cv, q, k, v, o, lse, fused, pf, s);
     if (RSWA_GQA_TC && gqa_tc_supported(cv))
       return launch_decode_gqa_tc(cv, q, k, v, o, lse, fused, pf, s);
     if (decode_gqa_heads_per_cta(cv) > 1)
@@ -612,6 +619,12 @@ cudaError_t launch_decode(const CacheView& cv, const void* q, const void* k,
 
 // Partial slots per (b, h) of the decode path launch_decode takes for cv.
 int decode_part_slots(const CacheView& cv) {
+  if (cv.H != cv.Hkv && !decode_use_small(cv) && RSWA_GQA_TC && RSWA_GQA_SK &&
+      gqa_sk_supported(cv)) {
+    // a KV head's partials: at most one per tile of its list
+    const int th = (int)((cv.m_cap + 127) / 128 + (cv.n + 127) / 128);
+    return std::max(cv.max_chunks, th + 1);
+  }
   if (!decode_use_small(cv) && RSWA_STREAM_DECODE && decode_use_stream(cv) &&
       !(cv.H != cv.Hkv && ((RSWA_GQA_TC && gqa_tc_supported(cv)) ||
                            decode_gqa_heads_per_cta(cv) > 1)))

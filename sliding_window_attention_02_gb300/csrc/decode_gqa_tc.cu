@@ -78,15 +78,6 @@ constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Byte offset of element (row r, column c) in a K-major bf16 operand made of
-// 64-column atoms of `atom` bytes, 128-byte swizzle (16-byte chunk index
-// XOR row mod 8).
-__device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
-  const int cc = c & 63;
-  return (uint32_t)(c >> 6) * atom + (uint32_t)r * 128u +
-         ((uint32_t)(((cc * 2) >> 4) ^ (r & 7)) << 4) + (uint32_t)((cc * 2) & 15);
-}
-
 // PREFETCH: the preceding kernel of the stream writes no prefix row, so a
 // prefix slot's first K and V tiles may be requested before the dependency
 // wait.

@@ -94,6 +94,12 @@ inline bool gqa_tc_shape(int heads, int kv_heads, int head_dim, int dtype) {
   return dtype == RSWA_BF16 && head_dim == 128 && per_kv >= 2 && per_kv <= 16;
 }
 bool gqa_tc_supported(const CacheView& cv);
+// Stream-K form of the grouped tensor-core decode (decode_gqa_sk.cu):
+// persistent CTAs split the key tiles of all KV heads evenly.
+bool gqa_sk_supported(const CacheView& cv);
+cudaError_t launch_decode_gqa_sk(const CacheView& cv, const void* q, const void* k,
+                                 const void* v, void* o, float* lse, bool fused,
+                                 bool prefetch_prefix, cudaStream_t s);
 // prefetch_prefix: the stream's preceding kernel writes no prefix row of
 // this cache (the first K/V tiles of prefix chunks load before its end).
 cudaError_t launch_decode_gqa_tc(const CacheView& cv, const void* q,

@@ -188,6 +188,15 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo,
   return d;
 }
 
+// Byte offset of element (row r, column c) in a K-major bf16 operand made of
+// 64-column atoms of `atom` bytes, 128-byte swizzle (16-byte chunk index
+// XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
+  const int cc = c & 63;
+  return (uint32_t)(c >> 6) * atom + (uint32_t)r * 128u +
+         ((uint32_t)(((cc * 2) >> 4) ^ (r & 7)) << 4) + (uint32_t)((cc * 2) & 15);
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 D, dense:
 // D format f32 (bits 4-5 = 1), A and B format bf16 (bits 7-9, 10-12 = 1),
 // B major-ness in bit 16 (0 = K-major, 1 = MN-major), N >> 3 in bits 17-22,

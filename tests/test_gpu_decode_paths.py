@@ -261,3 +261,60 @@ def test_decode_block_any_length(cuda_lib, case):
             f64(Vs[b, :, m_cap:])[:, held].transpose(1, 0, 2), st["Vr"][held])
         np.testing.assert_array_equal(f64(Ks[b, :, :m]).transpose(1, 0, 2), st["Kp"])
         assert cache.cache_len(b) == oracle.cache_len(m, n, T)
+
+
+GQA_TC_CASES = [
+    # (B, H, Hkv, m_lo, m_hi, n, T0): the tensor-core grouped decode's forms
+    (24, 32, 8, 100, 1500, 128, 130),     # stream-K: ragged heads split over CTAs
+    (3, 8, 2, 0, 40, 1024, 5),            # stream-K: tiny, most CTAs without work
+    (300, 8, 2, 50, 400, 64, 70),         # B > 256: one CTA per chunk
+    (24, 32, 2, 200, 900, 128, 20),       # 16 heads per KV head: one CTA per chunk
+    (16, 24, 8, 700, 2100, 256, 300),     # 3 heads per KV head, two-tile wrapped ring
+]
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("case", GQA_TC_CASES, ids=lambda c: f"B{c[0]}H{c[1]}kv{c[2]}n{c[5]}")
+def test_gqa_tc_forms(cuda_lib, case, fused):
+    """The grouped tensor-core decode in its stream-K form (persistent CTAs
+    over the key tiles of all KV heads) and its one-CTA-per-chunk form,
+    against the oracle over a few back-to-back steps."""
+    rswa = cuda_lib
+    B, H, Hkv, m_lo, m_hi, n, T0 = case
+    d, steps = 128, 3
+    m_list = workloads.prefix_lengths(B, m_lo, m_hi, seed=B + H)
+    rows = [m + T0 for m in m_list]
+    K = workloads.normal((sum(rows), Hkv, d), 321, 1.0, torch.bfloat16)
+    V = workloads.normal((sum(rows), Hkv, d), 322, 1.0, torch.bfloat16)
+    cache = rswa.RswaCache(max(m_list), n, H, d, B, rswa.RSWA_BF16, kv_heads=Hkv)
+    cache.prefill(None, K.cuda(), V.cuda(), None, m_list, T0)
+    offs = np.cumsum([0] + rows)
+    states = [oracle.prefill_cache(f64(K[offs[b]:offs[b + 1]]),
+                                   f64(V[offs[b]:offs[b + 1]]), m_list[b], n, T0)
+              for b in range(B)]
+    q_all = workloads.normal((steps * B, H, d), 323, 1.0, torch.bfloat16).cuda()
+    k_all = workloads.normal((steps * B, Hkv, d), 324, 1.0, torch.bfloat16).cuda()
+    v_all = workloads.normal((steps * B, Hkv, d), 325, 1.0, torch.bfloat16).cuda()
+    o = torch.empty(steps, B, H, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(steps, B, H, device="cuda")
+    for s in range(steps):
+        q, k, v = (x[s * B:(s + 1) * B] for x in (q_all, k_all, v_all))
+        if fused:
+            cache.decode_step_fused(q, k, v, o[s], lse[s])
+        else:
+            cache.append_kv(k, v)
+            cache.decode_step(q, o[s], lse[s])
+    torch.cuda.synchronize()
+    assert cache.sync_status() == 0
+    check = range(B) if B <= 32 else range(0, B, 13)
+    for s in range(steps):
+        got, gl = f64(o[s]), f64(lse[s])
+        for b in range(B):
+            sl = s * B + b
+            states[b], ro, rl = oracle.decode_step_fused(
+                states[b], f64(q_all[sl]), f64(k_all[sl]), f64(v_all[sl]), n)
+            if b in check:
+                assert_close(got[b], ro, 1, f"step {s} seq {b}")
+                assert np.abs(gl[b] - rl).max() <= 1e-3
+    for b in range(B):
+        assert cache.get_t(b) == T0 + steps
