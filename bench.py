@@ -48,6 +48,7 @@ KERNEL_SOURCES = {
     "decode_cluster_kernel": ["decode.cu", "attend.cuh", "rswa_device.cuh",
                               "tc_ptx.cuh"],
     "decode_gqa_tc_kernel": ["decode_gqa_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
+    "decode_gqa_sk_kernel": ["decode_gqa_sk.cu", "tc_ptx.cuh", "rswa_device.cuh"],
     "decode_stream_kernel": ["decode_stream.cu", "attend.cuh", "rswa_device.cuh",
                              "tc_ptx.cuh"],
     "block_tc_kernel": ["block_tc.cu", "tc_ptx.cuh", "rswa_device.cuh"],
@@ -1026,10 +1027,10 @@ def extra_rooflines(extras, peaks, peak_src):
                                   lp.get("kernel", "decode_kernel") + "@long_prefix"))
     gq = extras.get("batched_decode_gqa")
     if gq:
-        out.append(roofline_entry("decode_gqa_tc_kernel", "batched_decode_gqa",
+        out.append(roofline_entry("decode_gqa_sk_kernel", "batched_decode_gqa",
                                   "hbm", gq["algorithmic_bytes"], gq["us_per_step"],
                                   hbm, "hbm_gbs", peak_src,
-                                  "decode_gqa_tc_kernel@batched"))
+                                  "decode_gqa_sk_kernel@batched"))
     return out
 
 
