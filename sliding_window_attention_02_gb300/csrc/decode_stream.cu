@@ -53,19 +53,31 @@ constexpr int kWarps = RSWA_STREAM_WARPS;        // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kU = 4;                            // rows per lane group and stage
 constexpr int NS = RSWA_STREAM_STAGES;           // stages
-// Stages a CTA may request before its dependency wait: 2 measured best on
-// GB300 for the 40-page step (13.3 against 13.7 us per layer with all 6);
-// more early traffic slows the previous launch's combine.
+// Stages a CTA may request before its dependency wait: a third of its
+// stages, at least RSWA_STREAM_EARLY_STAGES and at most 4.  Measured on
+// GB300, one sequence through 12 layers (us per layer): 40 pages (11 stages
+// per CTA) 12.66 with 2 early stages, 12.48 with 3, 12.42 with 4; 16 pages
+// (5 stages) 8.13 with 1, 8.03 with 2, 8.25 with 3 — more early traffic
+// slows the previous launch's combine unless the CTA has much left to read.
 #ifndef RSWA_STREAM_EARLY_STAGES
 #define RSWA_STREAM_EARLY_STAGES 2
 #endif
 constexpr int kEarlyStages = RSWA_STREAM_EARLY_STAGES;
+constexpr int kEarlyStagesMax = 4;
 constexpr uint32_t kTensorStage = kWarps * kU * 512;   // K (or V) bytes of a stage
 constexpr uint32_t kStageBytes = 2 * kTensorStage;
 constexpr uint32_t OFF_BAR = NS * kStageBytes;
 constexpr uint32_t OFF_FLAG = OFF_BAR + 16 * NS;
 constexpr uint32_t kSmemBytes = OFF_FLAG + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Brings the 128-byte line holding p into L2; no other effect.  L2 is the
+// point of coherence for global memory, so a prefetch issued before the
+// programmatic dependency wait is safe even for data the preceding kernel
+// writes: the loads after the wait still see that kernel's stores.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
   uint4 r;
@@ -123,9 +135,12 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     span1 = min(total, span0 + share);
     nst = span1 > span0 ? (int)((span1 - span0 + SR - 1) / SR) : 0;
   };
-  // Copies stage k (ring slot `filled` and beyond are not copied); returns
-  // false once the bounded wait for a free slot gave up.
-  int64_t filled = 0;
+  // Copies stage k (ring slots from the first unfilled one on are not
+  // copied); returns false once the bounded wait for a free slot gave up.
+  // t_b is read after the dependency wait, and only stages that hold ring
+  // slots use it, so the producer's first stages do not wait for the load.
+  int64_t t_b = 0;
+  auto ring_filled = [&]() { return FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b); };
   auto issue = [&](int k) {
     const int s = k % NS;
     if (k >= NS && !ptx::mbar_wait(empty(s), ((k / NS) - 1) & 1, abort_flag,
@@ -133,10 +148,13 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
       return false;
     const int64_t l0 = span0 + (int64_t)k * SR, l1 = min(l0 + SR, span1);
     const int64_t p1 = min(l1, m_b);                    // prefix rows [l0, p1)
-    const int64_t r0 = max(l0, m_b) - m_b;              // ring slots [r0, r1)
-    const int64_t r1 = max(r0, min(l1 - m_b, filled));
     const uint32_t np = p1 > l0 ? (uint32_t)(p1 - l0) : 0u;
-    const uint32_t nr = (uint32_t)(r1 - r0);
+    int64_t r0 = 0;                                     // ring slots [r0, r1)
+    uint32_t nr = 0;
+    if (l1 > m_b) {
+      r0 = max(l0, m_b) - m_b;
+      nr = (uint32_t)(max(r0, min(l1 - m_b, ring_filled())) - r0);
+    }
     ptx::mbar_arrive_expect_tx(full(s), 2u * (np + nr) * ROW_B);
     const uint32_t kd = sb + (uint32_t)s * kStageBytes, vd = kd + kTensorStage;
     if (np) {
@@ -151,6 +169,19 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     return true;
   };
 
+  // The first accesses after the wait read a few lines each (q, t_b, the
+  // new key and value): have them in L2 by the time the wait returns.
+  if (producer) {
+    constexpr int QL = (D * (int)sizeof(T) + 127) / 128;  // lines per row
+    const char* pf = nullptr;
+    if (lane < QL) pf = reinterpret_cast<const char*>(q + bh * D) + lane * 128;
+    else if (lane == QL) pf = reinterpret_cast<const char*>(cv.t_dev + bh);
+    else if (FUSED && lane < 2 * QL + 1)
+      pf = reinterpret_cast<const char*>(knew + bkv * D) + (lane - QL - 1) * 128;
+    else if (FUSED && lane < 3 * QL + 1)
+      pf = reinterpret_cast<const char*>(vnew + bkv * D) + (lane - 2 * QL - 1) * 128;
+    if (pf) prefetch_l2(pf);
+  }
   int issued = 0;                                       // stages issued
   if (PREFETCH) {
     m_b = cv.m_dev[b];
@@ -158,7 +189,8 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     if (producer && lane == 0) {
       // Stages made only of prefix rows: their addresses and contents are
       // fixed until the next prefill.
-      while (issued < min(nst, kEarlyStages) &&
+      const int early = min(NS, max(kEarlyStages, min(kEarlyStagesMax, (nst + 1) / 3)));
+      while (issued < min(nst, early) &&
              min(span0 + (int64_t)(issued + 1) * SR, span1) <= m_b) {
         issue(issued);
         ++issued;
@@ -174,10 +206,7 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     plan();
   }
   if (nst == 0) return;                                 // no rows: nothing issued
-  const int64_t t_b = cv.t_dev[bh];
-  filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
-  const int64_t w = FUSED ? t_b % cv.n : -1;            // slot of the new key
-  const bool has_w = FUSED && span0 <= m_b + w && m_b + w < span1;
+  t_b = cv.t_dev[bh];
   const T* kn = FUSED ? knew + bkv * D : nullptr;
   const T* vn = FUSED ? vnew + bkv * D : nullptr;
 
@@ -191,6 +220,9 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
         ptx::mbar_wait(full(k % NS), (k / NS) & 1, never, kWaitLimitNs);
     }
   } else {
+    const int64_t filled = ring_filled();
+    const int64_t w = FUSED ? t_b % cv.n : -1;          // slot of the new key
+    const bool has_w = FUSED && span0 <= m_b + w && m_b + w < span1;
     if (has_w && h % grp == 0 && warp == 0) {
       // This CTA holds slot w: store the new key and value there.  The
       // copies of this launch that may read the slot race with the store, so
