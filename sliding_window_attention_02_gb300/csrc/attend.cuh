@@ -39,6 +39,24 @@ __device__ __forceinline__ void load_q_frag(const T* q_row, int lane,
   for (int e = 0; e < C::EPL; ++e) qf[e] *= sc;
 }
 
+// Evict-first L2 policy for keys and values a launch reads once (a cache
+// streamed from HBM): the streamed rows are the first victims, so they do not
+// displace the split-K partials, q and the per-sequence state.
+__device__ __forceinline__ uint64_t stream_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 16-byte load through the read-only path, no L1 allocation, with the L2
+// eviction policy `pol`.
+__device__ __forceinline__ uint4 ld_stream16_hint(const void* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
 // One batch of a warp's rows for attend_range: this lane's 16-byte slices
 // of the U rows of K and V its lane group takes, and which of them are keys.
 template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
@@ -49,12 +67,13 @@ struct AttendBatch {
 
 // Load the batch starting at logical row `base` (see attend_range for the
 // row mapping); rows at or past j_end are flagged and read row j_begin.
-template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
+// EVF: the rows are loaded with the L2 policy `pol` (stream_policy).
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL, bool EVF = false>
 __device__ __forceinline__ void attend_load(
     const T* __restrict__ Kb, const T* __restrict__ Vb, int64_t stride,
     int64_t base, int64_t j_begin, int64_t j_end, int64_t sub_row,
     const T* knew, const T* vnew, int lane, int64_t seg_end, int64_t gap,
-    AttendBatch<T, D, UNROLL>& bt) {
+    AttendBatch<T, D, UNROLL>& bt, uint64_t pol = 0) {
   using C = AttendCfg<T, D, UNROLL>;
   constexpr int EPL = C::EPL, LPK = C::LPK, KPW = C::KPW, U = C::U;
   const int grp = lane / LPK;
@@ -71,8 +90,13 @@ __device__ __forceinline__ void attend_load(
       kp = knew + col;
       vp = vnew + col;
     }
-    bt.k[u] = ld_stream16(kp);
-    bt.v[u] = ld_stream16(vp);
+    if constexpr (EVF) {
+      bt.k[u] = ld_stream16_hint(kp, pol);
+      bt.v[u] = ld_stream16_hint(vp, pol);
+    } else {
+      bt.k[u] = ld_stream16(kp);
+      bt.v[u] = ld_stream16(vp);
+    }
   }
 }
 
@@ -127,17 +151,17 @@ __device__ __forceinline__ void attend_consume(
 // table, e.g. the prefix rows and the ring slots of a cache slab).  This warp
 // takes the rows j_begin + first + it * step + (0 .. KEYS_WARP-1).  A row
 // whose physical index equals sub_row is read from (knew, vnew) instead.
-template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL>
+template <typename T, int D, int UNROLL = RSWA_DECODE_UNROLL, bool EVF = false>
 __device__ __forceinline__ void attend_range(
     const float* qf, const T* __restrict__ Kb, const T* __restrict__ Vb,
     int64_t stride, int64_t j_begin, int64_t j_end, int64_t first,
     int64_t step, int64_t sub_row, const T* knew, const T* vnew, int lane,
     SoftmaxState<AttendCfg<T, D>::EPL>& st, int64_t seg_end = INT64_MAX,
-    int64_t gap = 0) {
+    int64_t gap = 0, uint64_t pol = 0) {
   for (int64_t base = j_begin + first; base < j_end; base += step) {
     AttendBatch<T, D, UNROLL> bt;
-    attend_load<T, D, UNROLL>(Kb, Vb, stride, base, j_begin, j_end, sub_row, knew,
-                              vnew, lane, seg_end, gap, bt);
+    attend_load<T, D, UNROLL, EVF>(Kb, Vb, stride, base, j_begin, j_end, sub_row, knew,
+                                   vnew, lane, seg_end, gap, bt, pol);
     attend_consume<T, D, UNROLL>(qf, bt, st);
   }
 }

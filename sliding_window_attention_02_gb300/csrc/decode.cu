@@ -17,6 +17,34 @@
 
 namespace rswa {
 
+// Stores v at a with the L2 eviction priority of `pol` (a createpolicy
+// descriptor).
+__device__ __forceinline__ void st_hint(float* a, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol)
+               : "memory");
+}
+// Evict-last priority for a split-K partial: kept in L2 while the streamed
+// keys pass through, until the merge reads and discards it.
+__device__ __forceinline__ uint64_t partial_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Drops, without write-back, the L2 lines that lie wholly inside [lo, hi):
+// merged split-K partials, which nothing reads again before a later launch
+// rewrites them, would otherwise go back to DRAM when the streamed keys
+// evict them.  The lines at the two ends may hold another head's partials
+// and are kept.  Thread t of nt takes lines t, t + nt, ...; the caller has
+// made every read of the range complete (a barrier after the merge).
+__device__ __forceinline__ void discard_l2_inside(const void* lo, const void* hi, int t,
+                                                  int nt) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(lo) + 127) & ~uintptr_t(127);
+  const uintptr_t e = reinterpret_cast<uintptr_t>(hi) & ~uintptr_t(127);
+  for (uintptr_t p = a + (uintptr_t)t * 128; p < e; p += (uintptr_t)nt * 128)
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // At least 5 resident CTAs per SM: measured best on GB300 for the batched
 // and long-output workloads (it also steers the compiler to issue a warp's
 // loads ahead of their use).
@@ -39,6 +67,8 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
   const size_t bkv = (size_t)b * cv.Hkv + h / grp;
   const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
   const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
+  // Each key and value row is read once per launch.
+  const uint64_t pol = stream_policy();
   AttendBatch<T, D> pre;
   bool have_pre = false;
   int64_t m_b = 0;
@@ -48,8 +78,8 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     const int64_t j1 = min(j0 + cv.chunk, m_b);
     const int64_t base = j0 + (int64_t)warp * C::KEYS_WARP;
     if (j0 < m_b && base < j1) {                  // a prefix chunk with rows here
-      attend_load<T, D>(Kb, Vb, D, base, j0, j1, -1, nullptr, nullptr, lane,
-                        INT64_MAX, 0, pre);
+      attend_load<T, D, RSWA_DECODE_UNROLL, true>(Kb, Vb, D, base, j0, j1, -1, nullptr,
+                                                  nullptr, lane, INT64_MAX, 0, pre, pol);
       have_pre = true;
     }
   }
@@ -111,8 +141,9 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
     attend_consume<T, D>(qf, pre, st);
     first += (int64_t)NW * C::KEYS_WARP;
   }
-  attend_range<T, D>(qf, Kb, Vb, D, j0, j1, first, (int64_t)NW * C::KEYS_WARP, sub,
-                     kn, vn, lane, st);
+  attend_range<T, D, RSWA_DECODE_UNROLL, true>(qf, Kb, Vb, D, j0, j1, first,
+                                               (int64_t)NW * C::KEYS_WARP, sub, kn, vn, lane,
+                                               st, INT64_MAX, 0, pol);
   merge_groups<T, D>(st);
 
   // Merge the warps through shared memory.
@@ -151,10 +182,11 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
 
   // Publish this chunk's partial (m, l, acc[D]).
   float* P = cv.part + (bh * cv.max_chunks) * (D + 2);
-  if (tid < D) P[c * (D + 2) + 2 + tid] = A;
+  const uint64_t ppol = partial_policy();
+  if (tid < D) st_hint(P + c * (D + 2) + 2 + tid, A, ppol);
   if (tid == 0) {
-    P[c * (D + 2)] = M;
-    P[c * (D + 2) + 1] = Ls;
+    st_hint(P + c * (D + 2), M, ppol);
+    st_hint(P + c * (D + 2) + 1, Ls, ppol);
   }
   __syncthreads();
   __shared__ int s_last;
@@ -173,6 +205,8 @@ decode_kernel(CacheView cv, const T* __restrict__ q, const T* __restrict__ knew,
       // (b, h) read it before its own arrival.
       if (FUSED) cv.t_dev[bh] = t_b + 1;
     }
+    __syncthreads();
+    discard_l2_inside(P, P + (size_t)nch * (D + 2), tid, blockDim.x);
   }
 }
 

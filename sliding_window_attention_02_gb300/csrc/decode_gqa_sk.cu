@@ -98,6 +98,51 @@ constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// Stores v at a with the L2 eviction priority of `pol` (a createpolicy
+// descriptor).
+__device__ __forceinline__ void st_hint(float* a, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol)
+               : "memory");
+}
+// Evict-last priority for a split-K partial: kept in L2 while the streamed
+// keys pass through, until the merge reads and discards it.
+__device__ __forceinline__ uint64_t partial_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// A key or value tile is read once per launch: its TMA loads carry an
+// evict-first L2 policy, so the streamed tiles do not displace the partials,
+// q and the state.
+__device__ __forceinline__ uint64_t stream_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
+// Drops, without write-back, the L2 lines that lie wholly inside [lo, hi):
+// merged split-K partials, which nothing reads again before a later launch
+// rewrites them, would otherwise go back to DRAM when the streamed keys
+// evict them.  The lines at the two ends may hold another head's partials
+// and are kept.  Thread t of nt takes lines t, t + nt, ...; the caller has
+// made every read of the range complete (a barrier after the merge).
+__device__ __forceinline__ void discard_l2_inside(const void* lo, const void* hi, int t,
+                                                  int nt) {
+  const uintptr_t a = (reinterpret_cast<uintptr_t>(lo) + 127) & ~uintptr_t(127);
+  const uintptr_t e = reinterpret_cast<uintptr_t>(hi) & ~uintptr_t(127);
+  for (uintptr_t p = a + (uintptr_t)t * 128; p < e; p += (uintptr_t)nt * 128)
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // The CTA of `P` whose range holds tile t of `tot` (ranges [c tot / P,
 // (c + 1) tot / P)).
 __device__ __forceinline__ int owner(int64_t t, int64_t tot, int P) {
@@ -263,6 +308,7 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
   // Issues load p_idx (K or V of tile p_i of segment p_seg): whole tiles,
   // except a head's last prefix tile and its ring tiles, fetched as 8-row
   // boxes up to the last row that holds a key (at least one box).
+  const uint64_t kpol = stream_policy();
   auto p_issue = [&](int64_t filled) {
     const Seg& sg = segs[p_seg];
     const int s = p_idx % NS;
@@ -282,14 +328,14 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
     if (rows == BN) {
       const CUtensorMap* map = isv ? &tmV : &tmK;
       mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
-      tma_load_2d(dst, map, 0, y, bar(B_FULL + s));
-      tma_load_2d(dst + kSub, map, 64, y, bar(B_FULL + s));
+      tma_load_2d_hint(dst, map, 0, y, bar(B_FULL + s), kpol);
+      tma_load_2d_hint(dst + kSub, map, 64, y, bar(B_FULL + s), kpol);
     } else {
       const CUtensorMap* map = isv ? &tmV8 : &tmK8;
       mbar_arrive_expect_tx(bar(B_FULL + s), (uint32_t)rows * 256u);
       for (int r = 0; r < rows; r += 8) {
-        tma_load_2d(dst + r * 128, map, 0, y + r, bar(B_FULL + s));
-        tma_load_2d(dst + kSub + r * 128, map, 64, y + r, bar(B_FULL + s));
+        tma_load_2d_hint(dst + r * 128, map, 0, y + r, bar(B_FULL + s), kpol);
+        tma_load_2d_hint(dst + kSub + r * 128, map, 64, y + r, bar(B_FULL + s), kpol);
       }
     }
   };
@@ -644,14 +690,15 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
         continue;
       }
       const size_t stride = (size_t)cv.part_slots * (HD + 2);
+      const uint64_t pol = partial_policy();
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if (g >= per_kv) break;
         float* P = cv.part + (bh0 + g) * stride + (size_t)sg.slot * (HD + 2);
-        P[2 + e] = __uint_as_float(ov[g]);
+        st_hint(P + 2 + e, __uint_as_float(ov[g]), pol);
         if (e == 0) {
-          P[0] = mg[g];
-          P[1] = lg[g];
+          st_hint(P, mg[g], pol);
+          st_hint(P + 1, lg[g], pol);
         }
       }
       if (!epi_sync()) {
@@ -663,7 +710,8 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
         ok = false;
         break;
       }
-      if (*s_last) {
+      const bool merged = *s_last;
+      if (merged) {
         float M[G], L[G], A[G];
         merge_partials<G, (G <= 2 ? 2 : 1)>(cv.part + bh0 * stride, stride, sg.nparts, HD,
                                             e, per_kv, M, L, A);
@@ -684,6 +732,11 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
         ok = false;
         break;
       }
+      if (merged)
+        for (int g = 0; g < per_kv; ++g) {
+          const float* P0 = cv.part + (bh0 + g) * stride;
+          discard_l2_inside(P0, P0 + (size_t)sg.nparts * (HD + 2), e, 128);
+        }
     }
   }
 

@@ -71,6 +71,18 @@ constexpr uint32_t OFF_FLAG = OFF_BAR + 16 * NS;
 constexpr uint32_t kSmemBytes = OFF_FLAG + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// cp.async.bulk of `bytes` contiguous bytes into this CTA's shared memory
+// with the L2 eviction policy `pol`: the streamed rows are read once per
+// launch, so they go with evict-first priority (stream_policy).
+__device__ __forceinline__ void bulk_load_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 // Brings the 128-byte line holding p into L2; no other effect.  L2 is the
 // point of coherence for global memory, so a prefetch issued before the
 // programmatic dependency wait is safe even for data the preceding kernel
@@ -139,6 +151,7 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
   // copied); returns false once the bounded wait for a free slot gave up.
   // t_b is read after the dependency wait, and only stages that hold ring
   // slots use it, so the producer's first stages do not wait for the load.
+  const uint64_t pol = stream_policy();               // rows read once per launch
   int64_t t_b = 0;
   auto ring_filled = [&]() { return FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b); };
   auto issue = [&](int k) {
@@ -158,13 +171,13 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
     ptx::mbar_arrive_expect_tx(full(s), 2u * (np + nr) * ROW_B);
     const uint32_t kd = sb + (uint32_t)s * kStageBytes, vd = kd + kTensorStage;
     if (np) {
-      ptx::bulk_load(kd, Kb + l0 * D, np * ROW_B, full(s));
-      ptx::bulk_load(vd, Vb + l0 * D, np * ROW_B, full(s));
+      bulk_load_hint(kd, Kb + l0 * D, np * ROW_B, full(s), pol);
+      bulk_load_hint(vd, Vb + l0 * D, np * ROW_B, full(s), pol);
     }
     if (nr) {
       const uint32_t off = (uint32_t)(max(l0, m_b) - l0) * ROW_B;
-      ptx::bulk_load(kd + off, Kb + (cv.m_cap + r0) * D, nr * ROW_B, full(s));
-      ptx::bulk_load(vd + off, Vb + (cv.m_cap + r0) * D, nr * ROW_B, full(s));
+      bulk_load_hint(kd + off, Kb + (cv.m_cap + r0) * D, nr * ROW_B, full(s), pol);
+      bulk_load_hint(vd + off, Vb + (cv.m_cap + r0) * D, nr * ROW_B, full(s), pol);
     }
     return true;
   };
