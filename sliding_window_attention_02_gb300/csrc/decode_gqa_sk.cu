@@ -253,7 +253,6 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
   const int tid = threadIdx.x;
   const int per_kv = cv.H / cv.Hkv;                 // query heads per KV head (<= G)
   const int64_t n = cv.n;
-  const int rt = (int)((n + BN - 1) / BN);          // ring tiles per head
 
   if (tid == 0) {
     for (int k = 0; k < NBAR; ++k) {
@@ -753,8 +752,8 @@ decode_gqa_sk_kernel(const __grid_constant__ CUtensorMap tmK,
   if (tid == 0 && *abort_flag) flag_error(cv.err, kErrWaitTimeout);
 }
 
-// Persistent CTAs: RSWA_SK_GRID_PCT percent of two per SM.  95 measured best
-// on GB300 for the batched GQA step (59.3 us; 100: 60.5, 90: 60.4, 80: 63.0):
+// Persistent CTAs: RSWA_SK_GRID_PCT percent of two per SM; 95 measured best on
+// GB300, batched GQA step (53.6-53.9 us; 100: 54.5, 90: 54.9, 80: 57.8):
 // a few free slots let the next launch's CTAs become resident and request
 // their first tiles while this launch's last CTAs finish.
 #ifndef RSWA_SK_GRID_PCT
