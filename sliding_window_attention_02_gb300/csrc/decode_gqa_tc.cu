@@ -83,6 +83,23 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 // wait.
 // tmK8 / tmV8: the same slabs with 8-row boxes, for the rows of a chunk's
 // last tile (whole 8-row groups; the tile's other rows are not fetched).
+// A key or value tile is read once per launch: its TMA loads carry an
+// evict-first L2 policy, so the streamed tiles do not displace the partials,
+// q and the state.
+__device__ __forceinline__ uint64_t stream_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                                 int32_t y, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 template <bool FUSED, int G, bool PREFETCH>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -139,17 +156,18 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
   const int y = blockIdx.y;
   const size_t bkv = (size_t)b * cv.Hkv + kv;
   const bool spec = y < cp_cap;
+  const uint64_t kpol = stream_policy();
   auto spec_loads = [&]() {
     if (warp == kProducerWarp && lane == 0 && spec) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
       const int yr = (int)((int64_t)bkv * cv.slab_rows + (int64_t)y * chunk);
       mbar_arrive_expect_tx(bar(B_FULL + 0), kTileB);
-      tma_load_2d(sb + OFF_RING, &tmK, 0, yr, bar(B_FULL + 0));
-      tma_load_2d(sb + OFF_RING + kSub, &tmK, 64, yr, bar(B_FULL + 0));
+      tma_load_2d_hint(sb + OFF_RING, &tmK, 0, yr, bar(B_FULL + 0), kpol);
+      tma_load_2d_hint(sb + OFF_RING + kSub, &tmK, 64, yr, bar(B_FULL + 0), kpol);
       mbar_arrive_expect_tx(bar(B_FULL + 1), kTileB);
-      tma_load_2d(sb + OFF_RING + kTileB, &tmV, 0, yr, bar(B_FULL + 1));
-      tma_load_2d(sb + OFF_RING + kTileB + kSub, &tmV, 64, yr, bar(B_FULL + 1));
+      tma_load_2d_hint(sb + OFF_RING + kTileB, &tmV, 0, yr, bar(B_FULL + 1), kpol);
+      tma_load_2d_hint(sb + OFF_RING + kTileB + kSub, &tmV, 64, yr, bar(B_FULL + 1), kpol);
     }
   };
   if (PREFETCH) spec_loads();
@@ -214,14 +232,14 @@ decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmK,
     if (rows == BN) {
       const CUtensorMap* map = isv ? &tmV : &tmK;
       mbar_arrive_expect_tx(bar(B_FULL + s), kTileB);
-      tma_load_2d(dst, map, 0, y, bar(B_FULL + s));
-      tma_load_2d(dst + kSub, map, 64, y, bar(B_FULL + s));
+      tma_load_2d_hint(dst, map, 0, y, bar(B_FULL + s), kpol);
+      tma_load_2d_hint(dst + kSub, map, 64, y, bar(B_FULL + s), kpol);
     } else {
       const CUtensorMap* map = isv ? &tmV8 : &tmK8;
       mbar_arrive_expect_tx(bar(B_FULL + s), (uint32_t)rows * 256u);
       for (int r = 0; r < rows; r += 8) {
-        tma_load_2d(dst + r * 128, map, 0, y + r, bar(B_FULL + s));
-        tma_load_2d(dst + kSub + r * 128, map, 64, y + r, bar(B_FULL + s));
+        tma_load_2d_hint(dst + r * 128, map, 0, y + r, bar(B_FULL + s), kpol);
+        tma_load_2d_hint(dst + kSub + r * 128, map, 64, y + r, bar(B_FULL + s), kpol);
       }
     }
   };
