@@ -216,11 +216,12 @@ RSWA_API int rswa_decode_step_fused(rswa_cache* cache, const void* q,
  * t_b has advanced by `block`.  For verifying drafted tokens (a few tokens)
  * or prefilling output text into an existing cache (any length).
  * block == 1 runs rswa_decode_step_fused (same layouts), so the prefix
- * ordering rule of rswa_decode_step holds for every block size.  Larger
- * blocks take two kernels on `stream`: attention (on the tensor cores for
- * bf16, head_dim 128 and blocks of 64 or more; else on the CUDA cores), then
- * the append, which waits for the attention kernel to finish (the ring
- * slots it overwrites are read by the block's earlier outputs).
+ * ordering rule of rswa_decode_step holds for every block size.  The append
+ * follows every read of the ring (the slots it overwrites are read by the
+ * block's earlier outputs): blocks of 64 or more on a bf16, head_dim 128
+ * cache take two kernels on `stream`, attention on the tensor cores and then
+ * the append, which waits for it; shorter blocks (and other caches) take one
+ * kernel on the CUDA cores whose last CTA per KV head appends.
  * Errors: RSWA_EINVAL (block outside 1..2^24, batch above 65535, null or
  * misaligned pointers), RSWA_EHANDLE, RSWA_ECUDA.
  */
