@@ -26,14 +26,14 @@
 // lazily.  Every wait is bounded; on a timeout the CTA drains its copies and
 // MMAs, frees TMEM, sets the cache's device error flag and exits.
 //
-// A unit whose second half holds no row of the block (blocks of up to 128
-// tokens, and the last unit of some longer blocks) is split instead: both
-// halves take the first half's query rows, half 0 the even and half 1 the
-// odd key tiles of the unit, so the two halves still alternate on the tensor
-// core; at the end half 1 hands its (m, l, O) to half 0 through shared memory
-// and half 0 writes the merged rows (blocks of 64 / 128 tokens on the
-// single-page cache: 20.9 / 21.6 us per call as plain units, 17.1 / 17.5
-// split, the append kernel included).
+// When pairs of tiles would not fill the SMs once, a unit is one query tile
+// instead, split: both halves take its rows, half 0 the even and half 1 the
+// odd key tiles, so the two halves still alternate on the tensor core and
+// each CTA's chain of tiles is half as long; at the end half 1 hands its
+// (m, l, O) to half 0 through shared memory and half 0 writes the merged
+// rows.  So is the last unit of a pair grid whose second tile holds no row.
+// Single-page cache, per call with the append kernel: blocks of 64 / 256 /
+// 1024 tokens 20.7 / 26.1 / 26.9 us as pairs, 16.3 / 16.8 / 17.8 split.
 //
 // The cache is only read here; the append of the block's last min(n, C)
 // tokens runs afterwards (decode_block.cu), once this kernel has finished
@@ -101,8 +101,8 @@ struct Tiles {
   }
 };
 
-// Unit u: head u % H, then (sequence, tile pair) of the block.  split: the
-// second half holds no row of the block.
+// Unit u: head u % H, then (sequence, tile or tile pair) of the block.
+// split: the unit's second half holds no row of the block.
 struct Unit {
   int b, h, kvh, q0;
   bool split;
@@ -110,14 +110,16 @@ struct Unit {
   Tiles tl;
 };
 
-__device__ __forceinline__ Unit unit_at(int u, const CacheView& cv, int C) {
+// rows: 2 BM (a pair of query tiles per unit) or BM (one tile per unit, split
+// into the two halves).
+__device__ __forceinline__ Unit unit_at(int u, const CacheView& cv, int C, int rows) {
   Unit w;
-  const int pairs = (C + 2 * BM - 1) / (2 * BM);
+  const int per_head = (C + rows - 1) / rows;
   w.h = u % cv.H;
   const int rest = u / cv.H;
-  w.b = rest / pairs;
-  w.q0 = (rest % pairs) * 2 * BM;
-  w.split = w.q0 + BM >= C;
+  w.b = rest / per_head;
+  w.q0 = (rest % per_head) * rows;
+  w.split = rows == BM || w.q0 + BM >= C;       // no second tile in this unit
   w.kvh = w.h / (cv.H / cv.Hkv);
   w.m_b = cv.m_dev[w.b];
   w.t_b = cv.t_dev[(size_t)w.b * cv.H + w.h];
@@ -126,7 +128,7 @@ __device__ __forceinline__ Unit unit_at(int u, const CacheView& cv, int C) {
   // Rows i <= n - 2 see cached outputs (while t_b >= 1): all filled slots.
   const int64_t filled = min(n, w.t_b);
   w.tl.nr = (w.q0 <= n - 2 && filled > 0) ? (int)((filled + BN - 1) / BN) : 0;
-  const int q_hi = min(w.q0 + 2 * BM - 1, C - 1);
+  const int q_hi = min(w.q0 + rows - 1, C - 1);
   const int64_t lo = max((int64_t)0, (int64_t)w.q0 - n + 1);
   w.tl.kb0 = (int)(lo / BN);
   w.tl.nb = q_hi / BN - w.tl.kb0 + 1;
@@ -141,7 +143,7 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const __grid_constant__ CUtensorMap tmVc,
                 const __grid_constant__ CUtensorMap tmKb,
                 const __grid_constant__ CUtensorMap tmVb, CacheView cv, int C,
-                __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
+                int unit_rows, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
                 uint64_t wait_ns) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -172,7 +174,7 @@ block_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Unit w = unit_at(blockIdx.x, cv, C);
+  const Unit w = unit_at(blockIdx.x, cv, C, unit_rows);
   const int nt = w.tl.count();                  // >= 1: every row sees itself
 
   if (warp == kProducerWarp) {
@@ -608,9 +610,14 @@ cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
   cudaError_t e = cudaFuncSetAttribute(
       block_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int64_t units = (int64_t)cv.B * ((C + 2 * BM - 1) / (2 * BM)) * cv.H;
+  // Units of one query tile (each split over the two halves) while pairs of
+  // tiles would not fill the SMs once: twice the CTAs, each with half the
+  // key-tile chain.
+  const int64_t pair_units = (int64_t)cv.B * ((C + 2 * BM - 1) / (2 * BM)) * cv.H;
+  const int unit_rows = pair_units < cv.sms ? BM : 2 * BM;
+  const int64_t units = (int64_t)cv.B * ((C + unit_rows - 1) / unit_rows) * cv.H;
   block_tc_kernel<<<(unsigned)units, kThreads, kSmemBytes, s>>>(
-      mq, mkc, mvc, mkb, mvb, cv, C, static_cast<__nv_bfloat16*>(o), lse,
+      mq, mkc, mvc, mkb, mvb, cv, C, unit_rows, static_cast<__nv_bfloat16*>(o), lse,
       phase_wait_limit_ns());
   return cudaGetLastError();
 }

@@ -205,6 +205,7 @@ CHUNK_CASES = [
     ([300], 64, 3, 3, 128, 1, 20, [63, 64, 65]),             # around the TC threshold
     ([0], 128, 4, 4, 128, 1, 0, [64, 100]),                  # split units: 1, then 2 key tiles
     ([1056], 128, 4, 2, 128, 1, 200, [300]),                 # split last unit, wrapped ring, grouped
+    ([0, 17, 128, 129, 200, 255, 256, 300], 128, 10, 5, 128, 1, 40, [300]),  # paired tiles: 160 units fill the SMs
     ([100], 7, 2, 2, 64, 1, 3, [20, 9]),                     # d 64: CUDA cores
     ([50], 16, 2, 2, 128, 0, 9, [40]),                       # float32: CUDA cores
 ]
