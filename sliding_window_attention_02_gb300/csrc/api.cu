@@ -426,8 +426,10 @@ int rswa_decode_block(rswa_cache* cache, const void* q, const void* k,
       return launch_decode(cache->cv, q, k, v, o, lse, true, pf,
                            static_cast<cudaStream_t>(stream));
     });
-  return status_of(launch_decode_block(cache->cv, q, k, v, block, o, lse,
-                                       static_cast<cudaStream_t>(stream)));
+  return run_decode(cache, [&](bool pf) {
+    return launch_decode_block(cache->cv, q, k, v, block, o, lse, pf,
+                               static_cast<cudaStream_t>(stream));
+  });
 }
 
 int rswa_decode_step_fused_static(rswa_cache* cache, const void* q,

@@ -63,10 +63,13 @@ __device__ __forceinline__ void append_block_group(const CacheView& cv, const T*
 // them, NW * KEYS_WARP rows per round, and merge in shared memory.  8 warps
 // in general; 16 (one CTA per SM) when the grid fits one wave of the
 // device's SMs, so that each query takes half as many dependent row batches.
+// PREFETCH: the preceding kernel of the stream writes no prefix row and no
+// m_b of this cache (the host's per-handle flag), so each warp reads m_b and
+// loads its first batch of prefix rows before the dependency wait.
 constexpr int kBlockWarps = 8;
 constexpr int kBlockWarpsWide = 16;
 
-template <typename T, int D, int NW>
+template <typename T, int D, int NW, bool PREFETCH>
 __global__ void __launch_bounds__(NW * 32)
 decode_block_kernel(CacheView cv, const T* __restrict__ q,
                     const T* __restrict__ kblk, const T* __restrict__ vblk,
@@ -75,29 +78,42 @@ decode_block_kernel(CacheView cv, const T* __restrict__ q,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.y;
   const int64_t qi = blockIdx.x;                         // i * H + h
-  griddep_wait();
-  griddep_launch_dependents();
   const int64_t i = qi / cv.H;
   const int h = (int)(qi % cv.H);
   const size_t bh = (size_t)b * cv.H + h;
   const int kvh = h / (cv.H / cv.Hkv);
   const size_t bkv = (size_t)b * cv.Hkv + kvh;
-  const int64_t m_b = cv.m_dev[b];
+  const int64_t first = (int64_t)warp * C::KEYS_WARP;
+  const int64_t step = (int64_t)NW * C::KEYS_WARP;
+  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
+  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
+  int64_t m_b = 0;
+  AttendBatch<T, D> pre;
+  bool have_pre = false;
+  if (PREFETCH) {
+    m_b = cv.m_dev[b];
+    if (first < m_b) {
+      attend_load<T, D>(Kb, Vb, D, first, 0, m_b, -1, nullptr, nullptr, lane, INT64_MAX,
+                        0, pre);
+      have_pre = true;
+    }
+  }
+  griddep_wait();
+  griddep_launch_dependents();
+  if (!PREFETCH) m_b = cv.m_dev[b];
   const int64_t t_b = cv.t_dev[bh];
   const int64_t n = cv.n;
   const int64_t row_stride = (int64_t)cv.Hkv * D;        // k, v: [B][k][Hkv][D]
   const size_t qrow = ((size_t)b * k + i) * cv.H + h;    // q, o: [B][k][H][D]
-  const int64_t first = (int64_t)warp * C::KEYS_WARP;
-  const int64_t step = (int64_t)NW * C::KEYS_WARP;
 
   float qf[C::EPL];
   load_q_frag<T, D>(q + qrow * D, lane, qf);
   SoftmaxState<C::EPL> st;
   st.init();
-  const T* Kb = static_cast<const T*>(cv.K) + bkv * cv.slab_rows * D;
-  const T* Vb = static_cast<const T*>(cv.V) + bkv * cv.slab_rows * D;
-  // prefix
-  attend_range<T, D>(qf, Kb, Vb, D, 0, m_b, first, step, -1, nullptr, nullptr,
+  // prefix (the first batch already loaded with PREFETCH)
+  if (have_pre) attend_consume<T, D>(qf, pre, st);
+  attend_range<T, D>(qf, Kb, Vb, D, 0, m_b, have_pre ? first + step : first, step, -1,
+                     nullptr, nullptr,
                      lane, st);
   // cached outputs of the window: j in [j_lo, t_b), slot j mod n
   const int64_t j_lo = max((int64_t)0, t_b + i - n + 1);
@@ -211,41 +227,50 @@ static cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, cudaStream_t s,
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+template <typename T, int D, bool PF>
+static cudaError_t launch_block_cc(const CacheView& cv, const void* q, const void* k,
+                                   const void* v, int64_t block, void* o, float* lse,
+                                   cudaStream_t s) {
+  const int64_t nq = block * cv.H;
+  const dim3 grid((unsigned)nq, (unsigned)cv.B);
+  return nq * cv.B <= cv.sms
+             ? launch_pdl(decode_block_kernel<T, D, kBlockWarpsWide, PF>, grid,
+                          dim3(kBlockWarpsWide * 32), s, cv, (const T*)q, (const T*)k,
+                          (const T*)v, block, (T*)o, lse)
+             : launch_pdl(decode_block_kernel<T, D, kBlockWarps, PF>, grid,
+                          dim3(kBlockWarps * 32), s, cv, (const T*)q, (const T*)k,
+                          (const T*)v, block, (T*)o, lse);
+}
+
 template <typename T, int D>
 static cudaError_t launch_block_t(const CacheView& cv, const void* q,
                                   const void* k, const void* v, int64_t block,
-                                  void* o, float* lse, cudaStream_t s) {
+                                  void* o, float* lse, bool prefetch, cudaStream_t s) {
   cudaError_t e;
   if (block_tc_supported(cv, block)) {
-    e = launch_block_tc(cv, q, k, v, block, o, lse, s);
+    e = launch_block_tc(cv, q, k, v, block, o, lse, prefetch, s);
     if (e != cudaSuccess) return e;
     const int64_t kw = std::min<int64_t>(block, cv.n);
     return launch_pdl(append_block_kernel<T, D>, dim3((unsigned)kw, (unsigned)cv.B),
                       dim3(128), s, cv, (const T*)k, (const T*)v, (int)block);
   } else {
-    const int64_t nq = block * cv.H;
-    const dim3 grid((unsigned)nq, (unsigned)cv.B);
-    e = nq * cv.B <= cv.sms
-            ? launch_pdl(decode_block_kernel<T, D, kBlockWarpsWide>, grid,
-                         dim3(kBlockWarpsWide * 32), s, cv, (const T*)q, (const T*)k,
-                         (const T*)v, block, (T*)o, lse)
-            : launch_pdl(decode_block_kernel<T, D, kBlockWarps>, grid,
-                         dim3(kBlockWarps * 32), s, cv, (const T*)q, (const T*)k,
-                         (const T*)v, block, (T*)o, lse);
+    e = prefetch ? launch_block_cc<T, D, true>(cv, q, k, v, block, o, lse, s)
+                 : launch_block_cc<T, D, false>(cv, q, k, v, block, o, lse, s);
   }
   return e;
 }
 
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
                                 const void* v, int64_t block, void* o, float* lse,
-                                cudaStream_t s) {
+                                bool prefetch, cudaStream_t s) {
   if (cv.dtype == RSWA_F32) {
-    if (cv.d == 64) return launch_block_t<float, 64>(cv, q, k, v, block, o, lse, s);
-    return launch_block_t<float, 128>(cv, q, k, v, block, o, lse, s);
+    if (cv.d == 64)
+      return launch_block_t<float, 64>(cv, q, k, v, block, o, lse, prefetch, s);
+    return launch_block_t<float, 128>(cv, q, k, v, block, o, lse, prefetch, s);
   }
   if (cv.d == 64)
-    return launch_block_t<__nv_bfloat16, 64>(cv, q, k, v, block, o, lse, s);
-  return launch_block_t<__nv_bfloat16, 128>(cv, q, k, v, block, o, lse, s);
+    return launch_block_t<__nv_bfloat16, 64>(cv, q, k, v, block, o, lse, prefetch, s);
+  return launch_block_t<__nv_bfloat16, 128>(cv, q, k, v, block, o, lse, prefetch, s);
 }
 
 }  // namespace rswa

@@ -113,19 +113,21 @@ bool make_tmap_rows_bf16(CUtensorMap* map, const void* base, uint64_t cols,
 cudaError_t launch_decode_gqa(const CacheView& cv, const void* q, const void* k,
                               const void* v, void* o, float* lse, bool fused,
                               cudaStream_t s);
+// prefetch: the preceding kernel of the stream writes no prefix row and no
+// m_b of this cache (the kernels may read them before the dependency wait).
 cudaError_t launch_decode_block(const CacheView& cv, const void* q, const void* k,
                                 const void* v, int64_t block, void* o, float* lse,
-                                cudaStream_t s);
+                                bool prefetch, cudaStream_t s);
 // Blocks of at least kBlockTcMin tokens of a bf16, head_dim 128 cache run
 // their attention on the tensor cores (block_tc.cu); smaller blocks, and
 // other caches, one CTA per query on the CUDA cores (decode_block.cu), which
-// measured faster below 64 tokens on GB300 (single-page cache, 16 tokens:
-// 12.3 against ~30 us).
+// measured faster below 64 tokens on GB300 (single-page cache, 16 / 32
+// tokens: 10.2 / 15.5 against 16.5 / 16.8 us).
 constexpr int64_t kBlockTcMin = 64;
 bool block_tc_supported(const CacheView& cv, int64_t block);
 cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
                             const void* v, int64_t block, void* o, float* lse,
-                            cudaStream_t s);
+                            bool prefetch, cudaStream_t s);
 // prefetch_prefix: the preceding kernel of the stream writes no prefix row
 // and no m_b of this cache (every decode launch but the first after a
 // prefill); the cluster path then loads them before its dependency wait.
