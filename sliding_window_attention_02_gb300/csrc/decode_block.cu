@@ -248,7 +248,7 @@ static cudaError_t launch_block_t(const CacheView& cv, const void* q,
                                   void* o, float* lse, bool prefetch, cudaStream_t s) {
   cudaError_t e;
   if (block_tc_supported(cv, block)) {
-    e = launch_block_tc(cv, q, k, v, block, o, lse, prefetch, s);
+    e = launch_block_tc(cv, q, k, v, block, o, lse, s);
     if (e != cudaSuccess) return e;
     const int64_t kw = std::min<int64_t>(block, cv.n);
     return launch_pdl(append_block_kernel<T, D>, dim3((unsigned)kw, (unsigned)cv.B),

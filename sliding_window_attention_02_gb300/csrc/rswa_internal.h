@@ -127,7 +127,7 @@ constexpr int64_t kBlockTcMin = 64;
 bool block_tc_supported(const CacheView& cv, int64_t block);
 cudaError_t launch_block_tc(const CacheView& cv, const void* q, const void* k,
                             const void* v, int64_t block, void* o, float* lse,
-                            bool prefetch, cudaStream_t s);
+                            cudaStream_t s);
 // prefetch_prefix: the preceding kernel of the stream writes no prefix row
 // and no m_b of this cache (every decode launch but the first after a
 // prefill); the cluster path then loads them before its dependency wait.
