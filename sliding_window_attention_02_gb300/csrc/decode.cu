@@ -335,18 +335,20 @@ decode_cluster_kernel(CacheView cv, const T* __restrict__ q,
     }
   const int64_t filled = FUSED ? min(cv.n, t_b + 1) : min(cv.n, t_b);
   const int64_t sub = FUSED ? cv.m_cap + t_b % cv.n : -1;
-  if (FUSED && rank == 0 && h % grp == 0) {
-    // Lanes that hold slot sub replace what they loaded with (knew, vnew),
-    // so the value this write races with is never used.
-    T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + sub) * D;
-    T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + sub) * D;
-    constexpr int NV = D * sizeof(T) / 16;
-    for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
-      if (i < NV)
-        reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(knew + bkv * D)[i];
-      else
-        reinterpret_cast<uint4*>(Vw)[i - NV] =
-            reinterpret_cast<const uint4*>(vnew + bkv * D)[i - NV];
+  if constexpr (FUSED) {
+    if (rank == 0 && h % grp == 0) {
+      // Lanes that hold slot sub replace what they loaded with (knew,
+      // vnew), so the value this write races with is never used.
+      T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + (size_t)sub) * D;
+      T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + (size_t)sub) * D;
+      constexpr int NV = D * sizeof(T) / 16;
+      for (int i = threadIdx.x; i < 2 * NV; i += blockDim.x) {
+        if (i < NV)
+          reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(knew + bkv * D)[i];
+        else
+          reinterpret_cast<uint4*>(Vw)[i - NV] =
+              reinterpret_cast<const uint4*>(vnew + bkv * D)[i - NV];
+      }
     }
   }
   bool ok[U];

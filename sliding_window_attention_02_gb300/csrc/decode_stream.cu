@@ -241,8 +241,8 @@ decode_stream_kernel(CacheView cv, int S, const T* __restrict__ q,
       // copies of this launch that may read the slot race with the store, so
       // the consumers take row w from (knew, vnew) instead.
       constexpr int NV = D * (int)sizeof(T) / 16;
-      T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + cv.m_cap + w) * D;
-      T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + cv.m_cap + w) * D;
+      T* Kw = static_cast<T*>(cv.K) + (bkv * cv.slab_rows + (size_t)(cv.m_cap + w)) * D;
+      T* Vw = static_cast<T*>(cv.V) + (bkv * cv.slab_rows + (size_t)(cv.m_cap + w)) * D;
       for (int i = lane; i < 2 * NV; i += 32) {
         if (i < NV)
           reinterpret_cast<uint4*>(Kw)[i] = reinterpret_cast<const uint4*>(kn)[i];

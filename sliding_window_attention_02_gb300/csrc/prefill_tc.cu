@@ -57,11 +57,12 @@ constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr int NS = 4;                          // K/V ring slots
 constexpr uint32_t kSub = BM * 64 * 2;         // [128][64] bf16, 128B-swizzled
-constexpr uint32_t kTileB = 2 * kSub;          // [128][128] bf16 = 32 KB
+constexpr uint32_t kTileB = BM * HD * 2;       // [128][128] bf16 = 32 KB (2 kSub)
 constexpr uint32_t OFF_Q = 0;                  // Q0, Q1
 constexpr uint32_t OFF_RING = 2 * kTileB;
 constexpr uint32_t OFF_BAR = OFF_RING + NS * kTileB;
 constexpr uint32_t kSmemBytes = OFF_BAR + 256 + 1024;  // + 1 KB alignment slack
+static_assert(kTileB == 2 * kSub, "a tile is two 64-column swizzled halves");
 
 __host__ __device__ constexpr uint32_t tm_s(int half) { return half ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t tm_o(int half) { return half ? 384u : 256u; }
