@@ -273,6 +273,10 @@ GQA_TC_CASES = [
     (300, 8, 2, 50, 400, 64, 70),         # B > 256: one CTA per chunk
     (24, 32, 2, 200, 900, 128, 20),       # 16 heads per KV head: one CTA per chunk
     (16, 24, 8, 700, 2100, 256, 300),     # 3 heads per KV head, two-tile wrapped ring
+    (12, 16, 8, 300, 1500, 128, 140),     # stream-K, 2 heads per KV head (G = 2)
+    (10, 48, 6, 300, 1500, 128, 140),     # stream-K, 8 heads per KV head (G = 8)
+    (260, 4, 2, 20, 300, 64, 70),         # B > 256, one CTA per chunk, G = 2
+    (260, 16, 2, 20, 300, 64, 70),        # B > 256, one CTA per chunk, G = 8
 ]
 
 
